@@ -1,0 +1,190 @@
+"""CPU oracle for the GDN decode step and its ReplaySSM mode (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY. Only tests/, the package smoke check and the
+benchmark's CPU-baseline leg may import this package. It shares no code with
+the CUDA library: the arithmetic lives in gdn_oracle.c (plain C, fp64).
+
+Storage arrays follow hybrid_ssm_gated_gb300.workload: fp32 as float32, fp16 as
+float16, bf16 as uint16 bit patterns, and the oracle-only fp64 as float64.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from .build import build
+
+F32, BF16, F16, F64 = 0, 1, 2, 3
+CODE = {"f32": F32, "bf16": BF16, "f16": F16, "f64": F64}
+NPTYPE = {F32: np.float32, BF16: np.uint16, F16: np.float16, F64: np.float64}
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = C.CDLL(build())
+        P, I, I64, D = C.c_void_p, C.c_int, C.c_int64, C.c_double
+        sig = {
+            "orc_round": (D, [D, I]),
+            "orc_round_array": (None, [P, I64, I, P]),
+            "orc_load_array": (None, [P, I64, I, P]),
+            "orc_gating": (None, [D, D, D, D, P, P]),
+            "orc_l2norm": (None, [I, P, D, P]),
+            "orc_decode_head": (None, [I, I, P, I, P, P, P, I, D, D, P]),
+            "orc_decode_step": (I, [I, I, I, I, I, I64, P, I, P, P, P, P, P, P, I, P, P, P, I]),
+            "orc_replay_window": (I, [I, I, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
+            "orc_replay_flush": (I, [I, I, I, P, I, P, P, I, P, P, P, I]),
+            "orc_replay_rollback": (I, [P, I, I]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(_lib, name)
+            fn.restype = res
+            fn.argtypes = args
+    return _lib
+
+
+def _code(dt) -> int:
+    return CODE[dt] if isinstance(dt, str) else int(dt)
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _arr(x, dt) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=NPTYPE[_code(dt)])
+
+
+# ---------------------------------------------------------------- formats
+
+
+def round_to(x: np.ndarray, dtype) -> np.ndarray:
+    """Round fp64 values to a storage dtype; returns the storage array."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=NPTYPE[_code(dtype)])
+    lib().orc_round_array(_ptr(x), x.size, _code(dtype), _ptr(out))
+    return out
+
+
+def load(arr: np.ndarray, dtype) -> np.ndarray:
+    """Exact fp64 values of a storage array."""
+    arr = _arr(arr, dtype)
+    out = np.empty(arr.shape, dtype=np.float64)
+    lib().orc_load_array(_ptr(arr), arr.size, _code(dtype), _ptr(out))
+    return out
+
+
+def gating(A_log: float, dt_bias: float, a: float, b: float) -> tuple[float, float]:
+    al, be = C.c_double(), C.c_double()
+    lib().orc_gating(float(A_log), float(dt_bias), float(a), float(b), C.addressof(al), C.addressof(be))
+    return al.value, be.value
+
+
+def l2norm(x: np.ndarray, scale: float = 1.0) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    lib().orc_l2norm(x.size, _ptr(x), float(scale), _ptr(y))
+    return y
+
+
+# ---------------------------------------------------------------- decode
+
+
+def decode_head(S: np.ndarray, sdt, q, k, v, idt, alpha: float, beta: float) -> np.ndarray:
+    """One decode step of one head; S ([dv, dk] storage array) is updated in place."""
+    assert S.dtype == NPTYPE[_code(sdt)] and S.flags["C_CONTIGUOUS"]
+    dv, dk = S.shape
+    q, k, v = _arr(q, idt), _arr(k, idt), _arr(v, idt)
+    out = np.empty(dv, dtype=np.float64)
+    lib().orc_decode_head(dk, dv, _ptr(S), _code(sdt), _ptr(q), _ptr(k), _ptr(v), _code(idt),
+                          float(alpha), float(beta), _ptr(out))
+    return out
+
+
+def decode_step(pool: np.ndarray, sdt, slots, q, k, v, a, b, idt, A_log, dt_bias,
+                nthreads: int = 1) -> tuple[np.ndarray, int]:
+    """One decode step of a batch; pool [num_slots, Hv, dv, dk] is updated in place.
+
+    Returns (out [B, Hv, dv] fp64, number of (sequence, head) units whose slot
+    was out of range).
+    """
+    assert pool.dtype == NPTYPE[_code(sdt)] and pool.flags["C_CONTIGUOUS"]
+    num_slots, Hv, dv, dk = pool.shape
+    q, k, v, a, b = (_arr(x, idt) for x in (q, k, v, a, b))
+    B = int(np.asarray(slots).shape[0])
+    Hk = q.size // (B * dk)
+    slots = np.ascontiguousarray(slots, dtype=np.int32)
+    A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+    dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+    out = np.empty((B, Hv, dv), dtype=np.float64)
+    bad = lib().orc_decode_step(B, Hk, Hv, dk, dv, num_slots, _ptr(pool), _code(sdt), _ptr(slots),
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(idt),
+                                _ptr(A_log), _ptr(dt_bias), _ptr(out), int(nthreads))
+    return out, bad
+
+
+# ---------------------------------------------------------------- ReplaySSM
+
+
+class ReplayHead:
+    """ReplaySSM state of one (sequence, value head), as the oracle defines it.
+
+    S0: the checkpoint (storage dtype). Entries buffered since the checkpoint
+    are kept in arrival order (entry e is the e-th token after ckpt_pos):
+    raw k [L, dk] and v [L, dv] in the input dtype, alpha/beta [L] fp64.
+    meta = [count, pos, ckpt_pos].
+    """
+
+    def __init__(self, S0: np.ndarray, sdt, idt, L: int, pos: int = 0):
+        self.sdt, self.idt, self.L = _code(sdt), _code(idt), int(L)
+        self.S0 = np.ascontiguousarray(S0, dtype=NPTYPE[self.sdt]).copy()
+        self.dv, self.dk = self.S0.shape
+        self.ek = np.zeros((L, self.dk), dtype=NPTYPE[self.idt])
+        self.ev = np.zeros((L, self.dv), dtype=NPTYPE[self.idt])
+        self.ea = np.zeros(L, dtype=np.float64)
+        self.eb = np.zeros(L, dtype=np.float64)
+        self.meta = np.array([0, pos, pos], dtype=np.int32)
+
+    @property
+    def count(self) -> int:
+        return int(self.meta[0])
+
+    @property
+    def pos(self) -> int:
+        return int(self.meta[1])
+
+    @property
+    def ckpt_pos(self) -> int:
+        return int(self.meta[2])
+
+    def window(self, q, k, v, a, b, A_log: float, dt_bias: float) -> np.ndarray:
+        """Process T tokens (T = q.shape[0]); returns out [T, dv] fp64."""
+        q, k, v = _arr(q, self.idt), _arr(k, self.idt), _arr(v, self.idt)
+        T = q.shape[0]
+        a = np.ascontiguousarray(a, dtype=np.float64).reshape(T)
+        b = np.ascontiguousarray(b, dtype=np.float64).reshape(T)
+        out = np.empty((T, self.dv), dtype=np.float64)
+        rc = lib().orc_replay_window(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
+                                     _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                     _ptr(self.meta), T, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                     float(A_log), float(dt_bias), _ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle replay window rejected its input (code {rc})")
+        return out
+
+    def flush(self, force: bool = True) -> None:
+        rc = lib().orc_replay_flush(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
+                                    _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                    _ptr(self.meta), int(bool(force)))
+        if rc != 0:
+            raise ValueError(f"oracle replay flush rejected its state (code {rc})")
+
+    def rollback(self, T: int, accepted: int) -> None:
+        rc = lib().orc_replay_rollback(_ptr(self.meta), int(T), int(accepted))
+        if rc != 0:
+            raise ValueError(f"oracle rollback rejected its input (code {rc})")

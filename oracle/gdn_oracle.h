@@ -1,0 +1,72 @@
+/*
+ * gdn_oracle.h -- CPU oracle for the GDN (Gated DeltaNet) recurrent-state
+ * decode step and its ReplaySSM mode.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library; the product path
+ * (the CUDA library and its binding) never does, and shares no code with it.
+ *
+ * Conventions
+ *   - Storage dtype codes: 0 = fp32, 1 = bf16, 2 = fp16, 3 = fp64 (fp64 is an
+ *     oracle-only "no rounding" storage used for drift references).
+ *   - A head state S is dk x dv; it is stored column by column: element
+ *     (i, j) -- key index i, value index j -- sits at j*dk + i. A state pool
+ *     is [num_slots][Hv][dv][dk].
+ *   - Activations: q, k [B][Hk][dk]; v [B][Hv][dv]; a, b [B][Hv]; all in the
+ *     input dtype. A_log, dt_bias are fp32 [Hv]. Outputs are fp64.
+ *   - All arithmetic is fp64. A state is rounded (round-to-nearest-even) to
+ *     its storage dtype only when it is written back.
+ */
+#ifndef GDN_ORACLE_H
+#define GDN_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F16 = 2, ORC_F64 = 3 };
+
+/* Storage formats. */
+int orc_dtype_size(int dtype);
+double orc_round(double x, int dtype);
+double orc_load(const void* base, int64_t idx, int dtype);
+void orc_store(void* base, int64_t idx, int dtype, double x);
+void orc_round_array(const double* x, int64_t n, int dtype, void* out);
+void orc_load_array(const void* in, int64_t n, int dtype, double* out);
+
+/* Gating and normalisation. */
+void orc_gating(double A_log, double dt_bias, double a, double b, double* alpha, double* beta);
+void orc_l2norm(int n, const double* x, double scale, double* y);
+
+/* One decode step of one (sequence, value head). S is updated in place
+ * (rounded to sdt); out[dv] receives o = S_t^T q from the unrounded S_t. */
+void orc_decode_head(int dk, int dv, void* S, int sdt, const void* q, const void* k, const void* v,
+                     int idt, double alpha, double beta, double* out);
+
+/* One decode step of a batch through slot indices. Returns the number of
+ * (sequence, head) units whose slot was >= num_slots (skipped, output zero);
+ * slot < 0 is padding (skipped, output zero). */
+int orc_decode_step(int B, int Hk, int Hv, int dk, int dv, int64_t num_slots, void* pool, int sdt,
+                    const int32_t* slots, const void* q, const void* k, const void* v, const void* a,
+                    const void* b, int idt, const float* A_log, const float* dt_bias, double* out,
+                    int nthreads);
+
+/* ReplaySSM, one (sequence, value head). The replay state is the checkpoint
+ * S0 (dv*dk elements of sdt), the inputs of the entries buffered since the
+ * checkpoint in arrival order -- raw k [L][dk] and v [L][dv] in idt, gates
+ * alpha/beta [L] -- and meta = {count, pos, ckpt_pos}.
+ * Return 0, or a negative code: -1 bad T, -2 bad count, -3 bad accepted. */
+int orc_replay_window(int dk, int dv, int L, void* S0, int sdt, void* ek, void* ev, int idt,
+                      double* ealpha, double* ebeta, int32_t* meta, int T, const void* q,
+                      const void* k, const void* v, const double* a, const double* b, double A_log,
+                      double dt_bias, double* out);
+int orc_replay_flush(int dk, int dv, int L, void* S0, int sdt, const void* ek, const void* ev,
+                     int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force);
+int orc_replay_rollback(int32_t* meta, int T, int accepted);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
