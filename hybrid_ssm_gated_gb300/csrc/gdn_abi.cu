@@ -1,0 +1,202 @@
+// gdn_abi.cu -- the extern "C" entry points declared in include/gdn.h:
+// argument validation on the host, then one kernel launch on the caller's
+// stream. Nothing here allocates, synchronises or logs.
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "../../include/gdn.h"
+#include "gdn_dispatch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int launched(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) {
+        g_last_error.clear();
+        return GDN_OK;
+    }
+    if (e == cudaErrorNotSupported) return fail(GDN_ERR_SHAPE, "%s: no kernel for this dtype/dk", what);
+    return fail(GDN_ERR_LAUNCH, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, int n) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)n) == 0; }
+bool dtype_ok(int32_t d) { return d == GDN_F32 || d == GDN_BF16 || d == GDN_F16; }
+
+int check_dims(const gdn_dims* d, const char* fn) {
+    if (!d) return fail(GDN_ERR_NULL, "%s: dims is NULL", fn);
+    if (d->B < 0 || d->Hk <= 0 || d->Hv <= 0 || d->num_slots < 0)
+        return fail(GDN_ERR_SHAPE, "%s: negative or zero sizes (B=%d Hk=%d Hv=%d num_slots=%lld)", fn, d->B, d->Hk,
+                    d->Hv, (long long)d->num_slots);
+    if (d->Hv % d->Hk != 0) return fail(GDN_ERR_SHAPE, "%s: Hv=%d is not a multiple of Hk=%d", fn, d->Hv, d->Hk);
+    if (d->dk != 32 && d->dk != 64 && d->dk != 128)
+        return fail(GDN_ERR_SHAPE, "%s: dk=%d not in {32, 64, 128}", fn, d->dk);
+    if (d->dv < 16 || d->dv > gdn::DV_MAX || d->dv % 16 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: dv=%d must be a multiple of 16 in [16, 256]", fn, d->dv);
+    if ((int64_t)d->B * d->Hv > (int64_t)INT32_MAX / 8)
+        return fail(GDN_ERR_SHAPE, "%s: B*Hv=%lld too large", fn, (long long)d->B * d->Hv);
+    return GDN_OK;
+}
+
+// Rows of a state per 16 KB chunk: the largest power-of-two divisor of dv
+// that keeps a chunk within CHUNK_BYTES.
+void chunking(int dk, int dv, int state_bytes, int& rows, int& nchunk) {
+    rows = gdn::CHUNK_BYTES / (dk * state_bytes);
+    if (rows > dv) rows = dv;
+    while (dv % rows != 0) rows /= 2;
+    nchunk = dv / rows;
+}
+
+int check_activations(const char* fn, const void* q, const void* k, const void* v, const void* a, const void* b,
+                      int32_t in_dtype, const float* A_log, const float* dt_bias, const void* out,
+                      int32_t out_dtype) {
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !out)
+        return fail(GDN_ERR_NULL, "%s: an activation / parameter / output pointer is NULL", fn);
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+        return fail(GDN_ERR_DTYPE, "%s: unsupported dtype (in=%d out=%d)", fn, in_dtype, out_dtype);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+        return fail(GDN_ERR_ALIGN, "%s: q, k and v must be 16-byte aligned", fn);
+    const int isz = gdn::dtype_size(in_dtype), osz = gdn::dtype_size(out_dtype);
+    if (!aligned_to(a, isz) || !aligned_to(b, isz) || !aligned_to(out, osz) || !aligned_to(A_log, 4) ||
+        !aligned_to(dt_bias, 4))
+        return fail(GDN_ERR_ALIGN, "%s: a, b, A_log, dt_bias or out misaligned for its dtype", fn);
+    return GDN_OK;
+}
+
+int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* c, const int32_t* slots, int32_t T,
+                  int32_t force, const void* q, const void* k, const void* v, const void* a, const void* b,
+                  int32_t in_dtype, const float* A_log, const float* dt_bias, void* out, int32_t out_dtype,
+                  int32_t* dev_err, void* stream) {
+    int rc = check_dims(dims, fn);
+    if (rc) return rc;
+    if (!c) return fail(GDN_ERR_NULL, "%s: cache is NULL", fn);
+    if (dims->B == 0) return GDN_OK;
+    if (!c->ckpt || !c->ring_k || !c->ring_v || !c->ring_rec || !c->pos || !c->ckpt_pos || !slots || !dev_err)
+        return fail(GDN_ERR_NULL, "%s: a cache, slots or dev_err pointer is NULL", fn);
+    if (!dtype_ok(c->ckpt_dtype) || !dtype_ok(c->ring_dtype))
+        return fail(GDN_ERR_DTYPE, "%s: unsupported cache dtype (ckpt=%d ring=%d)", fn, c->ckpt_dtype, c->ring_dtype);
+    if (c->L < 1 || c->L > gdn::L_MAX) return fail(GDN_ERR_WINDOW, "%s: L=%d not in [1, 32]", fn, c->L);
+    if (T > 0) {
+        if (T > c->L || T > gdn::WINDOW_MAX)
+            return fail(GDN_ERR_WINDOW, "%s: window T=%d exceeds min(L=%d, 8)", fn, T, c->L);
+        rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
+        if (rc) return rc;
+        if (in_dtype != c->ring_dtype)
+            return fail(GDN_ERR_DTYPE, "%s: in_dtype=%d differs from the ring dtype %d", fn, in_dtype, c->ring_dtype);
+    } else if (T < 0) {
+        return fail(GDN_ERR_WINDOW, "%s: negative window", fn);
+    }
+    if (!aligned16(c->ckpt) || !aligned16(c->ring_k) || !aligned16(c->ring_v) || !aligned16(c->ring_rec) ||
+        !aligned_to(c->pos, 4) || !aligned_to(c->ckpt_pos, 4) || !aligned_to(slots, 4) || !aligned_to(dev_err, 4))
+        return fail(GDN_ERR_ALIGN, "%s: cache arrays must be 16-byte aligned", fn);
+
+    gdn::ReplayArgs p{};
+    p.ckpt = c->ckpt, p.ring_k = c->ring_k, p.ring_v = c->ring_v, p.ring_rec = c->ring_rec;
+    p.pos = c->pos, p.ckpt_pos = c->ckpt_pos, p.slots = slots;
+    p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias;
+    p.out = out, p.dev_err = dev_err;
+    p.num_slots = dims->num_slots;
+    p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.L = c->L, p.T = T, p.force = force != 0;
+    p.in_dtype = c->ring_dtype, p.out_dtype = T > 0 ? out_dtype : GDN_F32;
+    p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
+    chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
+    const int tmax = T <= 1 ? 1 : (T <= 4 ? 4 : 8);
+    bool too_big = false;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (c->ckpt_dtype == GDN_F32)
+        e = gdn::dispatch_replay_f32(dims->dk, tmax, p, s, too_big);
+    else if (c->ckpt_dtype == GDN_BF16)
+        e = gdn::dispatch_replay_bf16(dims->dk, tmax, p, s, too_big);
+    else
+        e = gdn::dispatch_replay_f16(dims->dk, tmax, p, s, too_big);
+    if (too_big) return fail(GDN_ERR_SHAPE, "%s: L=%d, T=%d, dv=%d do not fit in shared memory", fn, c->L, T, dims->dv);
+    return launched(e, fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_decode_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* slots, const void* q,
+                    const void* k, const void* v, const void* a, const void* b, int32_t in_dtype, const float* A_log,
+                    const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {
+    const char* fn = "gdn_decode_step";
+    int rc = check_dims(dims, fn);
+    if (rc) return rc;
+    if (dims->B == 0) return GDN_OK;
+    if (!state_pool || !slots || !dev_err) return fail(GDN_ERR_NULL, "%s: state_pool, slots or dev_err is NULL", fn);
+    if (!dtype_ok(state_dtype)) return fail(GDN_ERR_DTYPE, "%s: unsupported state dtype %d", fn, state_dtype);
+    rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
+    if (rc) return rc;
+    if (!aligned16(state_pool) || !aligned_to(slots, 4) || !aligned_to(dev_err, 4))
+        return fail(GDN_ERR_ALIGN, "%s: state_pool must be 16-byte aligned", fn);
+    gdn::DecodeArgs p{};
+    p.pool = state_pool, p.slots = slots, p.q = q, p.k = k, p.v = v, p.a = a, p.b = b;
+    p.A_log = A_log, p.dt_bias = dt_bias, p.out = out, p.dev_err = dev_err;
+    p.num_slots = dims->num_slots;
+    p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv;
+    p.in_dtype = in_dtype, p.out_dtype = out_dtype;
+    p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
+    chunking(dims->dk, dims->dv, gdn::dtype_size(state_dtype), p.rows, p.nchunk);
+    return launched(gdn::dispatch_decode(state_dtype, dims->dk, p, static_cast<cudaStream_t>(stream)), fn);
+}
+
+int gdn_replay_step(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* q,
+                    const void* k, const void* v, const void* a, const void* b, int32_t in_dtype, const float* A_log,
+                    const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {
+    return replay_common("gdn_replay_step", dims, cache, slots, 1, 0, q, k, v, a, b, in_dtype, A_log, dt_bias, out,
+                         out_dtype, dev_err, stream);
+}
+
+int gdn_verify_window(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t T,
+                      const void* q, const void* k, const void* v, const void* a, const void* b, int32_t in_dtype,
+                      const float* A_log, const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err,
+                      void* stream) {
+    if (T < 1) return fail(GDN_ERR_WINDOW, "gdn_verify_window: T=%d must be >= 1", T);
+    return replay_common("gdn_verify_window", dims, cache, slots, T, 0, q, k, v, a, b, in_dtype, A_log, dt_bias, out,
+                         out_dtype, dev_err, stream);
+}
+
+int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t force,
+                     int32_t* dev_err, void* stream) {
+    return replay_common("gdn_replay_flush", dims, cache, slots, 0, force, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         cache ? cache->ring_dtype : GDN_F32, nullptr, nullptr, nullptr, GDN_F32, dev_err, stream);
+}
+
+int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const int32_t* accepted,
+                 int32_t T, int32_t* dev_err, void* stream) {
+    const char* fn = "gdn_rollback";
+    int rc = check_dims(dims, fn);
+    if (rc) return rc;
+    if (!cache) return fail(GDN_ERR_NULL, "%s: cache is NULL", fn);
+    if (dims->B == 0) return GDN_OK;
+    if (!cache->pos || !cache->ckpt_pos || !slots || !accepted || !dev_err)
+        return fail(GDN_ERR_NULL, "%s: pos, ckpt_pos, slots, accepted or dev_err is NULL", fn);
+    if (T < 1 || T > cache->L || T > gdn::WINDOW_MAX)
+        return fail(GDN_ERR_WINDOW, "%s: T=%d not in [1, min(L, 8)]", fn, T);
+    return launched(gdn::launch_rollback(cache->pos, cache->ckpt_pos, slots, accepted, dims->B, dims->Hv, T,
+                                         dims->num_slots, dev_err, static_cast<cudaStream_t>(stream)),
+                    fn);
+}
+
+const char* gdn_last_error_string(void) { return g_last_error.c_str(); }
+
+int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,260 @@
+// gdn_decode.cuh -- the gated delta-rule decode step (gdn_decode_step).
+//
+// Rule (standard gated delta rule; the vLLM PR #52191 summary, section
+// 实现拆解 items 3-4, fixes its numeric contract: FP32 arithmetic, state
+// stored as fp32/bf16/fp16 and rounded once per write-back):
+//   S_t = alpha S_{t-1} + beta k (v - alpha S_{t-1}^T k)^T,   o_t = S_t^T q.
+// A dk x dv state is stored as dv rows ("columns of S") of dk contiguous
+// elements, so for row j:
+//   u_j = S[:,j].k   p_j = S[:,j].q   delta_j = beta (v_j - alpha u_j)
+//   S'[:,j] = alpha S[:,j] + k delta_j     o_j = alpha p_j + (q.k) delta_j
+// One read and one write of the state; ~4 FP32 ops per state element, so the
+// step is bound by HBM bandwidth, not by arithmetic.
+//
+// Kernel shape: persistent CTAs over (sequence, value head) units, one
+// producer warp + NCW consumer warps.
+//  - The producer warp fetches slot indices and gates for 32 units at a time
+//    (one lane per unit), then lane 0 streams each unit's state in 16 KB
+//    chunks into an NS-deep shared-memory ring with bulk copies on the TMA
+//    engine (cp.async.bulk + mbarrier transaction counts), together with the
+//    unit's q/k/v rows into an NH-deep "head" ring.
+//  - Consumer warps read the chunk from shared memory (128-bit, conflict
+//    free), do the fused update in FP32 registers, and store the new state
+//    (packed to the storage type) and the output straight to global memory.
+//    A row is covered by LPR = dk/16 lanes holding 16 elements each; the two
+//    row dot products are reduced with log2(LPR) xor-shuffles.
+//  - Every wait is bounded (GDN_DEVERR_TIMEOUT, then return).
+#pragma once
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+
+struct DecodeArgs {
+    void* pool;
+    const int32_t* slots;
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* a;
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+    void* out;
+    int32_t* dev_err;
+    int64_t num_slots;
+    int B, Hk, Hv, dv;
+    int in_dtype, out_dtype;
+    int rows;    // state rows per chunk
+    int nchunk;  // dv / rows
+    float q_scale;
+};
+
+constexpr int CHUNK_BYTES = 16384;
+constexpr int DV_MAX = 256;
+
+template <typename ST, int DK, int NCW, int NS, int NH>
+struct DecodeCfg {
+    static constexpr int VEC = Store<ST>::VEC;  // elements per 16-byte vector
+    static constexpr int E = 16;                // state elements per lane per row
+    static constexpr int NC = E / VEC;          // 16-byte vectors per lane per row
+    static constexpr int LPR = DK / E;          // lanes per row
+    static constexpr int RPP = 32 / LPR;        // rows per warp pass
+    static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
+    // head stage: meta (16 B) | q row | k row (DK fp32 max each) | v row (DV_MAX fp32 max)
+    static constexpr int OFF_Q = 16;
+    static constexpr int OFF_K = OFF_Q + DK * 4;
+    static constexpr int OFF_V = OFF_K + DK * 4;
+    static constexpr int HEAD = align_up(OFF_V + DV_MAX * 4, 128);
+    static constexpr int SMEM = NS * CHUNK_BYTES + NH * HEAD + (2 * NS + 2 * NH) * 8;
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static_assert(DK % E == 0 && LPR <= 32, "dk must be a multiple of 16 and at most 512");
+};
+
+template <typename ST, int DK, int NCW, int NS, int NH>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeArgs p) {
+    using C = DecodeCfg<ST, DK, NCW, NS, NH>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* chunks = smem;
+    unsigned char* heads = smem + NS * CHUNK_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(heads + NH * C::HEAD);
+    uint64_t* cfull = bars;
+    uint64_t* cempty = bars + NS;
+    uint64_t* hfull = bars + 2 * NS;
+    uint64_t* hempty = bars + 2 * NS + NH;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&cfull[s], 1), mbar_init(&cempty[s], NCW);
+        for (int s = 0; s < NH; ++s) mbar_init(&hfull[s], 1), mbar_init(&hempty[s], NCW);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int total = p.B * p.Hv;
+    const int in_sz = dtype_size(p.in_dtype);
+    const int group = p.Hv / p.Hk;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        const uint64_t pol = policy_evict_first();
+        const uint32_t qbytes = DK * in_sz, vbytes = p.dv * in_sz;
+        const uint32_t cbytes = p.rows * C::ROW_BYTES;
+        uint32_t m = 0;   // chunk fills issued
+        uint32_t nh = 0;  // head fills issued
+        int n = 0;        // units visited
+        bool ok = true;
+        for (int n0 = 0; ok && blockIdx.x + n0 * gridDim.x < total; n0 += 32) {
+            // lane l fetches the slot and gates of unit n0 + l
+            const int my_unit = blockIdx.x + (n0 + lane) * gridDim.x;
+            int slot = -1;
+            float alpha = 0.f, beta = 0.f;
+            if (my_unit < total) {
+                const int b = my_unit / p.Hv, h = my_unit - b * p.Hv;
+                const int s = p.slots[b];
+                if (s >= p.num_slots) {
+                    set_error(p.dev_err, GDN_DEVERR_SLOT);
+                } else if (s >= 0) {
+                    slot = s;
+                    gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, my_unit, p.in_dtype),
+                          load_elem(p.b, my_unit, p.in_dtype), alpha, beta);
+                }
+            }
+            for (int i = 0; i < 32; ++i, ++n) {
+                const int unit = blockIdx.x + n * gridDim.x;
+                if (unit >= total) break;
+                const int s_i = __shfl_sync(FULL_MASK, slot, i);
+                const float al = __shfl_sync(FULL_MASK, alpha, i);
+                const float be = __shfl_sync(FULL_MASK, beta, i);
+                if (lane == 0) {
+                    const int hs = n % NH;
+                    if (n >= NH) ok = mbar_wait(&hempty[hs], ((n / NH) + 1) & 1);
+                    if (ok) {
+                        unsigned char* head = heads + hs * C::HEAD;
+                        reinterpret_cast<int*>(head)[0] = s_i;
+                        reinterpret_cast<float*>(head)[1] = al;
+                        reinterpret_cast<float*>(head)[2] = be;
+                        if (s_i >= 0) {
+                            const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
+                            mbar_arrive_expect_tx(&hfull[hs], 2 * qbytes + vbytes);
+                            const int64_t qrow = (int64_t)b * p.Hk + kh;
+                            bulk_load(head + C::OFF_Q, static_cast<const char*>(p.q) + qrow * qbytes, qbytes,
+                                      &hfull[hs]);
+                            bulk_load(head + C::OFF_K, static_cast<const char*>(p.k) + qrow * qbytes, qbytes,
+                                      &hfull[hs]);
+                            bulk_load(head + C::OFF_V, static_cast<const char*>(p.v) + (int64_t)unit * vbytes,
+                                      vbytes, &hfull[hs]);
+                            const char* src = static_cast<const char*>(p.pool) +
+                                              ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES;
+                            for (int c = 0; c < p.nchunk; ++c, ++m) {
+                                const int cs = m % NS;
+                                if (m >= NS && !(ok = mbar_wait(&cempty[cs], ((m / NS) + 1) & 1))) break;
+                                mbar_arrive_expect_tx(&cfull[cs], cbytes);
+                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src + (int64_t)c * cbytes, cbytes,
+                                               &cfull[cs], pol);
+                            }
+                        } else {
+                            mbar_arrive(&hfull[hs]);
+                        }
+                        ++nh;
+                    }
+                }
+                ok = __shfl_sync(FULL_MASK, ok, 0);
+                if (!ok) break;
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.dev_err, GDN_DEVERR_TIMEOUT);
+            // let every copy already issued land before the CTA can exit
+            for (uint32_t s = 0; s < NS && s < m; ++s) mbar_wait(&cfull[s], ((m - 1 - s) / NS) & 1);
+            for (uint32_t s = 0; s < NH && s < nh; ++s) mbar_wait(&hfull[s], ((nh - 1 - s) / NH) & 1);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int pg = lane % C::LPR;        // lane's position within its row group
+    const int rsub = lane / C::LPR;      // row within the warp pass
+    const int passes = p.rows / C::RPP;  // warp passes per chunk
+    uint32_t m = 0;
+    for (int n = 0;; ++n) {
+        const int unit = blockIdx.x + n * gridDim.x;
+        if (unit >= total) break;
+        const int hs = n % NH;
+        if (!mbar_wait(&hfull[hs], (n / NH) & 1)) {
+            if (lane == 0) set_error(p.dev_err, GDN_DEVERR_TIMEOUT);
+            return;
+        }
+        const unsigned char* head = heads + hs * C::HEAD;
+        const int slot = reinterpret_cast<const int*>(head)[0];
+        const float alpha = reinterpret_cast<const float*>(head)[1];
+        const float beta = reinterpret_cast<const float*>(head)[2];
+        if (slot < 0) {
+            for (int j = cw * 32 + lane; j < p.dv; j += NCW * 32)
+                store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, 0.f);
+        } else {
+            // normalised k and q at this lane's 16 key positions
+            float kn[C::E], qn[C::E];
+#pragma unroll
+            for (int c = 0; c < C::NC; ++c) {
+                const int first = (c * C::LPR + pg) * C::VEC;
+                load_run<C::VEC>(head + C::OFF_K, first, p.in_dtype, kn + c * C::VEC);
+                load_run<C::VEC>(head + C::OFF_Q, first, p.in_dtype, qn + c * C::VEC);
+            }
+            float ssk = 0.f, ssq = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::E; ++e) ssk = fmaf(kn[e], kn[e], ssk), ssq = fmaf(qn[e], qn[e], ssq);
+            ssk = group_sum<C::LPR>(ssk);
+            ssq = group_sum<C::LPR>(ssq);
+            const float ik = rsqrtf(ssk + 1e-6f), iq = rsqrtf(ssq + 1e-6f) * p.q_scale;
+            float qk = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::E; ++e) kn[e] *= ik, qn[e] *= iq, qk = fmaf(kn[e], qn[e], qk);
+            qk = group_sum<C::LPR>(qk);
+
+            const int b = unit / p.Hv, h = unit - b * p.Hv;
+            char* gstate = static_cast<char*>(p.pool) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
+            for (int c = 0; c < p.nchunk; ++c, ++m) {
+                const int cs = m % NS;
+                if (!mbar_wait(&cfull[cs], (m / NS) & 1)) {
+                    if (lane == 0) set_error(p.dev_err, GDN_DEVERR_TIMEOUT);
+                    return;
+                }
+                const unsigned char* tile = chunks + cs * CHUNK_BYTES;
+                for (int ps = cw; ps < passes; ps += NCW) {
+                    const int r = ps * C::RPP + rsub;
+                    const int j = c * p.rows + r;
+                    float s[C::E];
+#pragma unroll
+                    for (int cc = 0; cc < C::NC; ++cc) {
+                        const uint4 raw = *reinterpret_cast<const uint4*>(tile + r * C::ROW_BYTES +
+                                                                          (cc * C::LPR + pg) * 16);
+                        Store<ST>::unpack(raw, s + cc * C::VEC);
+                    }
+                    float u = 0.f, pq = 0.f;
+#pragma unroll
+                    for (int e = 0; e < C::E; ++e) u = fmaf(s[e], kn[e], u), pq = fmaf(s[e], qn[e], pq);
+                    u = group_sum<C::LPR>(u);
+                    pq = group_sum<C::LPR>(pq);
+                    const float vj = load_elem(head + C::OFF_V, j, p.in_dtype);
+                    const float delta = beta * (vj - alpha * u);
+#pragma unroll
+                    for (int e = 0; e < C::E; ++e) s[e] = fmaf(kn[e], delta, alpha * s[e]);
+                    char* dst = gstate + (int64_t)j * C::ROW_BYTES;
+#pragma unroll
+                    for (int cc = 0; cc < C::NC; ++cc)
+                        *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = Store<ST>::pack(s + cc * C::VEC);
+                    if (pg == 0)
+                        store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, fmaf(alpha, pq, qk * delta));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cempty[cs]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hempty[hs]);
+    }
+}
+
+}  // namespace gdn

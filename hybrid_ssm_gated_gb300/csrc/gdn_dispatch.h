@@ -1,0 +1,24 @@
+// gdn_dispatch.h -- runtime dtype/shape -> kernel instantiation dispatch.
+// Each dispatcher lives in its own translation unit so the instantiations
+// compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gdn_decode.cuh"
+#include "gdn_replay.cuh"
+
+namespace gdn {
+
+// Returns cudaErrorNotSupported when (state dtype, dk) has no instantiation.
+cudaError_t dispatch_decode(int state_dtype, int dk, const DecodeArgs& a, cudaStream_t stream);
+
+// tmax in {1, 4, 8}. too_big is set when the layout does not fit in shared memory.
+cudaError_t dispatch_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_replay_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+
+cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
+                            int B, int Hv, int T, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,57 @@
+// Instantiations of the decode kernel (state dtype x dk) and the rollback launch.
+#include "gdn_dispatch.h"
+#include "gdn_launch.cuh"
+
+namespace gdn {
+
+// gdn_rollback: keep 1 + accepted[b] of the T window tokens of sequence b.
+__global__ void rollback_kernel(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
+                                int B, int Hv, int T, int64_t num_slots, int32_t* dev_err) {
+    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < B * Hv; u += gridDim.x * blockDim.x) {
+        const int b = u / Hv, h = u - b * Hv;
+        const int s = slots[b];
+        if (s < 0) continue;
+        if (s >= num_slots) {
+            if (h == 0) set_error(dev_err, GDN_DEVERR_SLOT);
+            continue;
+        }
+        const int acc = accepted[b];
+        if (acc < 0 || acc > T - 1) {
+            if (h == 0) set_error(dev_err, GDN_DEVERR_ACCEPT);
+            continue;
+        }
+        const int64_t idx = (int64_t)s * Hv + h;
+        const int np = pos[idx] - (T - 1 - acc);
+        if (np < ckpt_pos[idx]) {
+            set_error(dev_err, GDN_DEVERR_RING);
+            continue;
+        }
+        pos[idx] = np;
+    }
+}
+
+cudaError_t dispatch_decode(int state_dtype, int dk, const DecodeArgs& a, cudaStream_t s) {
+#define GDN_DEC(CODE, ST)                                  \
+    if (state_dtype == CODE) {                             \
+        if (dk == 32) return launch_decode<ST, 32>(a, s);  \
+        if (dk == 64) return launch_decode<ST, 64>(a, s);  \
+        if (dk == 128) return launch_decode<ST, 128>(a, s); \
+    }
+    GDN_DEC(GDN_F32, float)
+    GDN_DEC(GDN_BF16, __nv_bfloat16)
+    GDN_DEC(GDN_F16, __half)
+#undef GDN_DEC
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
+                            int B, int Hv, int T, int64_t num_slots, int32_t* dev_err, cudaStream_t s) {
+    const int n = B * Hv;
+    const int threads = 256;
+    int blocks = (n + threads - 1) / threads;
+    if (blocks > 1024) blocks = 1024;
+    rollback_kernel<<<blocks, threads, 0, s>>>(pos, ckpt_pos, slots, accepted, B, Hv, T, num_slots, dev_err);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

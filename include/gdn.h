@@ -1,0 +1,197 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) GDN recurrent-state decode library.
+ *
+ * The library runs one data-parallel hot path: the recurrent-state decode
+ * step of a Gated DeltaNet (GDN) linear-attention layer -- the gated delta
+ * rule that vLLM's fused sigmoid-gating delta-rule update kernel runs -- and
+ * its ReplaySSM mode.
+ *
+ * Sources. The vLLM PR #52191 summary on prhub ("CPU AMX GDN state FP16/BF16
+ * persistence, prefix caching +35%") names the decode kernel and its numeric
+ * contract in section 实现拆解, items 3-4: arithmetic in FP32, the state kept
+ * in fp32/bf16/fp16 and rounded once per write-back. It does not write out the
+ * rule, so the standard gated delta rule is used. Per sequence b and value
+ * head h, with key head kh = h / (Hv / Hk):
+ *     alpha = exp(-exp(A_log[h]) * softplus(a[b,h] + dt_bias[h]))
+ *     beta  = sigmoid(b[b,h])
+ *     k = k[b,kh] / sqrt(|k[b,kh]|^2 + 1e-6)
+ *     q = q[b,kh] / sqrt(|q[b,kh]|^2 + 1e-6) / sqrt(dk)
+ *     S_t = alpha S_{t-1} + beta k (v[b,h] - alpha S_{t-1}^T k)^T    (S: dk x dv)
+ *     o_t = S_t^T q
+ * softplus(x) = x for x > 20, else log(1 + e^x). The ReplaySSM mode is the
+ * one the AREX article on ReplaySSM describes in its section "缓存输入而非
+ * 状态：checkpoint 每 L 步才更新一次": a checkpoint S0 plus a buffer of the
+ * last tokens' state-building inputs; outputs are computed from S0 and the
+ * buffer without writing the state; the buffer is folded into S0 when full;
+ * rejected draft tokens are dropped by moving the buffer pointer.
+ *
+ * Conventions for every entry point
+ *   - Asynchronous: work is enqueued on `stream` (a cudaStream_t, NULL = the
+ *     legacy default stream). Nothing synchronises, allocates or logs.
+ *   - The caller owns all memory. Every pointer is a device pointer unless
+ *     noted, aligned to 16 bytes, to C-contiguous data with the layout given.
+ *   - Return value: GDN_OK, or a negative GDN_ERR_* code when the arguments
+ *     are rejected on the host (nothing is launched then) or a launch fails;
+ *     gdn_last_error_string() describes the last failure on this thread.
+ *   - Problems only visible on the device (a slot index >= num_slots, a
+ *     replay pointer pair out of range, an accepted count out of range, a
+ *     pipeline wait that timed out) set bits GDN_DEVERR_* in *dev_err with
+ *     atomicOr; the affected (sequence, head) is skipped and, where it has an
+ *     output, its output is zero-filled. Nothing traps. dev_err is required;
+ *     the caller clears it and reads it back when convenient.
+ *   - Slot indices are int32; a negative slot is padding: no state is read
+ *     or written and the output rows are zero. Slots within one call must be
+ *     distinct (not checked; duplicates race).
+ *   - Shapes: dk in {32, 64, 128}; dv a multiple of 16 in [16, 256];
+ *     Hv a multiple of Hk; B >= 0 (B == 0 launches nothing).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Host-side return codes. */
+#define GDN_OK 0
+#define GDN_ERR_NULL (-1)    /* a required pointer is NULL */
+#define GDN_ERR_DTYPE (-2)   /* unsupported dtype or dtype mismatch */
+#define GDN_ERR_SHAPE (-3)   /* unsupported dk/dv, Hv % Hk != 0, negative sizes */
+#define GDN_ERR_WINDOW (-4)  /* T < 1, T > L, T > 8, L > 32 */
+#define GDN_ERR_ALIGN (-5)   /* a pointer is not 16-byte aligned */
+#define GDN_ERR_LAUNCH (-6)  /* CUDA reported an error at launch */
+
+/* Device-side error bits (set in *dev_err). */
+#define GDN_DEVERR_SLOT 1    /* slot index >= num_slots */
+#define GDN_DEVERR_RING 2    /* replay count pos - ckpt_pos outside [0, L], or a rollback below ckpt_pos */
+#define GDN_DEVERR_ACCEPT 4  /* accepted count outside [0, T-1] */
+#define GDN_DEVERR_TIMEOUT 8 /* an internal pipeline wait gave up (should never happen) */
+
+/* Element types of states, activations and outputs; mirrors the fp32 /
+ * bf16 / fp16 choice of a mamba SSM cache dtype. */
+enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 };
+
+/* Problem sizes. B: sequences in the call; Hk / Hv: key / value heads;
+ * dk / dv: key / value head dimensions; num_slots: slots in the state pool. */
+typedef struct gdn_dims {
+    int32_t B, Hk, Hv, dk, dv;
+    int64_t num_slots;
+} gdn_dims;
+
+/*
+ * gdn_decode_step -- one gated delta-rule decode step for a batch of
+ * sequences whose states live in a paged pool (vLLM PR #52191 summary,
+ * 实现拆解 3-4: state_t storage, FP32 arithmetic, one rounding per
+ * write-back).
+ *
+ * state_pool  [num_slots][Hv][dv][dk] of state_dtype. Element (i, j) of the
+ *             dk x dv state of (slot, h) -- key index i, value index j -- is
+ *             at ((slot*Hv + h)*dv + j)*dk + i. Read, updated, rounded
+ *             (round-to-nearest-even) and written back in place.
+ * slots       [B] int32, slot of each sequence (< 0: padding).
+ * q, k        [B][Hk][dk] of in_dtype.   v: [B][Hv][dv];  a, b: [B][Hv].
+ * A_log, dt_bias  [Hv] fp32.
+ * out         [B][Hv][dv] of out_dtype: o_t, computed from the unrounded S_t.
+ * dev_err     int32 error word (see GDN_DEVERR_*).
+ */
+int gdn_decode_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype,
+                    const int32_t* slots, const void* q, const void* k, const void* v,
+                    const void* a, const void* b, int32_t in_dtype, const float* A_log,
+                    const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err,
+                    void* stream);
+
+/*
+ * ReplaySSM cache (AREX ReplaySSM article, "缓存输入而非状态"). Everything is
+ * indexed by slot and value head; each (slot, h) is an independent unit with
+ * its own checkpoint, L-entry ring and pointers.
+ *
+ * ckpt      [num_slots][Hv][dv][dk] of ckpt_dtype: the checkpoint S0, same
+ *           layout as a decode state pool. Written only when folded.
+ * ring_k    [num_slots][Hv][L][dk] of ring_dtype: raw (unnormalised) keys.
+ * ring_v    [num_slots][Hv][L][dv] of ring_dtype: raw values.
+ * ring_rec  [num_slots][Hv][L][4 + dv] fp32: per entry {alpha, beta, 0, 0,
+ *           w[0..dv)}, where alpha and beta are the entry's gates and
+ *           w = beta (v - alpha S_prev^T k) is the entry's correction vector
+ *           (S_prev: the state just before the entry). w is derived data the
+ *           kernels keep so that an output needs one pass over S0, not one
+ *           per buffered entry; it stays valid until the entry is folded.
+ * pos       [num_slots][Hv] int32: absolute position of the next token.
+ * ckpt_pos  [num_slots][Hv] int32: position the checkpoint corresponds to.
+ *           count = pos - ckpt_pos entries are buffered, 0 <= count <= L;
+ *           entry for absolute position t sits at ring index t mod L.
+ * L         ring length, 1 <= L <= 32.
+ *
+ * A fresh sequence: ckpt = its initial state, pos = ckpt_pos (any value >= 0).
+ * A fold -- ckpt <- round(S after all buffered entries), ckpt_pos <- pos --
+ * happens exactly when appending the call's tokens would overflow the ring
+ * (count + T > L), before they are appended, or on gdn_replay_flush.
+ */
+typedef struct gdn_replay_cache {
+    void* ckpt;
+    int32_t ckpt_dtype;
+    void* ring_k;
+    void* ring_v;
+    int32_t ring_dtype;
+    float* ring_rec;
+    int32_t* pos;
+    int32_t* ckpt_pos;
+    int32_t L;
+} gdn_replay_cache;
+
+/*
+ * gdn_replay_step -- one ReplaySSM standard-decode step: o_t = S_t^T q_t with
+ * S_t rebuilt in FP32 from S0 and the ring, the token's inputs appended, and
+ * no state written unless the ring was full (then it is folded first).
+ * Arguments as gdn_decode_step; in_dtype must equal cache->ring_dtype.
+ * Equivalent to gdn_verify_window with T = 1.
+ */
+int gdn_replay_step(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                    const void* q, const void* k, const void* v, const void* a, const void* b,
+                    int32_t in_dtype, const float* A_log, const float* dt_bias, void* out,
+                    int32_t out_dtype, int32_t* dev_err, void* stream);
+
+/*
+ * gdn_verify_window -- ReplaySSM speculative verify (AREX ReplaySSM article,
+ * "缓存输入而非状态": the draft window is checked in one pass from the cache).
+ * T tokens per sequence (the last verified token plus T-1 drafts), 1 <= T <=
+ * min(L, 8). Output j reads the state after window tokens 0..j. All T
+ * tokens are appended (pos += T); none of them is ever folded by this call.
+ * q, k  [B][T][Hk][dk];  v [B][T][Hv][dv];  a, b [B][T][Hv];
+ * out   [B][T][Hv][dv].
+ */
+int gdn_verify_window(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                      int32_t T, const void* q, const void* k, const void* v, const void* a,
+                      const void* b, int32_t in_dtype, const float* A_log, const float* dt_bias,
+                      void* out, int32_t out_dtype, int32_t* dev_err, void* stream);
+
+/*
+ * gdn_replay_flush -- fold the ring into the checkpoint for the given slots:
+ * every (slot, h) with count == L, or with count > 0 when force != 0.
+ */
+int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                     int32_t force, int32_t* dev_err, void* stream);
+
+/*
+ * gdn_rollback -- after a T-token verify, keep 1 + accepted[b] tokens of
+ * sequence b: pos[slot][h] -= T - 1 - accepted[b] for every head. A pure
+ * pointer move (AREX ReplaySSM article: rollback becomes moving the buffer
+ * pointer); no state or ring entry is touched.
+ * accepted  [B] int32 device array, each in [0, T-1].
+ */
+int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                 const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream);
+
+/* Text of the last host-side failure on the calling thread ("" if none). */
+const char* gdn_last_error_string(void);
+
+/* GDN_ABI_VERSION of the loaded library. */
+int32_t gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

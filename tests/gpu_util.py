@@ -1,0 +1,76 @@
+"""Shared helpers for the GPU parity tests (inputs to device, oracle on units)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from hybrid_ssm_gated_gb300 import gdn
+from hybrid_ssm_gated_gb300 import workload as wl
+
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+# Tolerances of the parity bar: max-abs 1e-4 with an fp32 state, atol 1e-2 with a
+# bf16/fp16 state (the atol the vLLM PR #52191 summary's decode tests use).
+TOL = {"f32": 1e-4, "bf16": 1e-2, "f16": 1e-2}
+
+
+def dev(arr: np.ndarray, dt: str) -> torch.Tensor:
+    return wl.to_torch(arr, dt).cuda()
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def host_values(arr: np.ndarray, dt: str) -> np.ndarray:
+    return wl.values(arr, dt)
+
+
+def step_to_device(x: dict, dt: str) -> dict:
+    return {k: dev(v, dt) for k, v in x.items()}
+
+
+def dev_err() -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def decode_oracle_unit(S: np.ndarray, sdt: str, x: dict, idt: str, b: int, h: int, Hv: int, Hk: int,
+                       A_log, dt_bias) -> np.ndarray:
+    """One oracle decode step of unit (b, h) on its state S (updated in place)."""
+    kh = h // (Hv // Hk)
+    al, be = oracle.gating(A_log[h], dt_bias[h], wl.values(x["a"][b, 0, h], idt), wl.values(x["b"][b, 0, h], idt))
+    return oracle.decode_head(S, sdt, x["q"][b, 0, kh], x["k"][b, 0, kh], x["v"][b, 0, h], idt, al, be)
+
+
+def sample_units(B: int, Hv: int, n: int, seed: int = 123) -> list[tuple[int, int]]:
+    r = np.random.default_rng(seed)
+    picks = {(0, 0), (B - 1, Hv - 1)}
+    while len(picks) < min(n, B * Hv):
+        picks.add((int(r.integers(B)), int(r.integers(Hv))))
+    return sorted(picks)
+
+
+def maxabs(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64)))) if np.size(a) else 0.0
+
+
+class GpuReplay:
+    """A ReplaySSM cache on the GPU built from a workload's initial pool."""
+
+    def __init__(self, w: wl.Workload, pool_host: np.ndarray):
+        num_slots = pool_host.shape[0]
+        self.cache = gdn.ReplayCache.allocate(num_slots, w.Hv, w.dk, w.dv, w.L, TORCH_DT[w.state_dtype],
+                                              TORCH_DT[w.in_dtype])
+        self.cache.ckpt.copy_(dev(pool_host, w.state_dtype))
+        self.w = w
+
+
+def replay_oracle_heads(w: wl.Workload, pool_host: np.ndarray, slots: np.ndarray, units) -> dict:
+    return {(b, h): oracle.ReplayHead(pool_host[slots[b], h], w.state_dtype, w.in_dtype, w.L) for b, h in units}
+
+
+def oracle_window(head: oracle.ReplayHead, x: dict, w: wl.Workload, b: int, h: int, A_log, dt_bias) -> np.ndarray:
+    kh = h // (w.Hv // w.Hk)
+    return head.window(q=x["q"][b, :, kh], k=x["k"][b, :, kh], v=x["v"][b, :, h],
+                       a=wl.values(x["a"][b, :, h], w.in_dtype), b=wl.values(x["b"][b, :, h], w.in_dtype),
+                       A_log=float(A_log[h]), dt_bias=float(dt_bias[h]))

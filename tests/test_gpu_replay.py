@@ -1,0 +1,210 @@
+"""GPU parity of the ReplaySSM entry points (gdn_replay_step, gdn_verify_window,
+gdn_replay_flush, gdn_rollback) against the CPU oracle.
+
+The oracle keeps, per (sequence, head), the checkpoint and the raw inputs
+buffered since it and rebuilds the state for every output; the kernels use a
+ring with derived correction vectors. Outputs and checkpoints are compared
+within the parity tolerances; the ring pointers and the raw k/v ring entries
+are compared bit-exactly; the stored gates within 1e-5 relative (they come
+from expf/log1pf in FP32 on the GPU and fp64 libm in the oracle, and the
+composition exp(-exp(A) softplus(x)) amplifies the relative error of its
+argument by |exp(A) softplus(x)| <= ~20).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_ssm_gated_gb300 import build, gdn
+from hybrid_ssm_gated_gb300 import workload as wl
+from tests.gpu_util import (TOL, TORCH_DT, GpuReplay, dev, dev_err, maxabs, oracle_window, replay_oracle_heads,
+                            sample_units, step_to_device, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+PREFILL = 100000  # step-seed offset of the pre-fill tokens
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    gdn.lib()
+
+
+class Harness:
+    def __init__(self, w: wl.Workload, units=None):
+        self.w = w
+        self.pool = wl.initial_pool(w)
+        self.slots = wl.slots(w)
+        self.A_log, self.dt_bias = wl.head_params(w)
+        self.g = GpuReplay(w, self.pool)
+        self.units = units if units is not None else [(b, h) for b in range(w.B) for h in range(w.Hv)]
+        self.heads = replay_oracle_heads(w, self.pool, self.slots, self.units)
+        self.A_d = torch.from_numpy(self.A_log).cuda()
+        self.dt_d = torch.from_numpy(self.dt_bias).cuda()
+        self.err = dev_err()
+        self.worst = 0.0
+
+    def window(self, x: dict, slots: np.ndarray, T: int, label: str):
+        w = self.w
+        xd = step_to_device(x, w.in_dtype)
+        out = torch.full((w.B, T, w.Hv, w.dv), 3.0, device="cuda")
+        s_d = torch.from_numpy(slots).cuda()
+        if T == 1:
+            gdn.gdn_replay_step(self.g.cache, s_d, xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], self.A_d, self.dt_d,
+                                out, self.err)
+        else:
+            gdn.gdn_verify_window(self.g.cache, s_d, xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], self.A_d, self.dt_d,
+                                  out, self.err)
+        got = to_f64(out)
+        for (b, h) in self.units:
+            if slots[b] < 0:
+                assert np.all(got[b, :, h] == 0.0)
+                continue
+            ref = oracle_window(self.heads[(b, h)], x, w, b, h, self.A_log, self.dt_bias)
+            d = maxabs(got[b, :, h], ref)
+            assert d <= TOL[w.state_dtype], f"{label} unit {(b, h)}: max |diff| {d:.3e}"
+            self.worst = max(self.worst, d)
+
+    def rollback(self, accepted: np.ndarray, T: int):
+        gdn.gdn_rollback(self.g.cache, torch.from_numpy(self.slots).cuda(), torch.from_numpy(accepted).cuda(), T,
+                         self.err)
+        for (b, h) in self.units:
+            self.heads[(b, h)].rollback(T, int(accepted[b]))
+
+    def prefill(self, offsets: np.ndarray):
+        for s in range(int(offsets.max(initial=0))):
+            x = wl.step_inputs(self.w.with_(T=1), PREFILL + s)
+            self.window(x, np.where(offsets > s, self.slots, -1).astype(np.int32), 1, f"prefill {s}")
+
+    def check_state(self):
+        """Checkpoints within tolerance; pointers and raw ring entries bit-exact."""
+        w, c = self.w, self.g.cache
+        torch.cuda.synchronize()
+        pos, ck = c.pos.cpu().numpy(), c.ckpt_pos.cpu().numpy()
+        rk = c.ring_k.view(torch.int16).cpu().numpy() if w.in_dtype != "f32" else c.ring_k.cpu().numpy()
+        rv = c.ring_v.view(torch.int16).cpu().numpy() if w.in_dtype != "f32" else c.ring_v.cpu().numpy()
+        rec = c.ring_rec.cpu().numpy()
+        for (b, h) in self.units:
+            hd, s = self.heads[(b, h)], self.slots[b]
+            assert (pos[s, h], ck[s, h]) == (hd.pos, hd.ckpt_pos), f"pointers of {(b, h)}"
+            S0 = to_f64(c.ckpt[s, h])
+            d = maxabs(S0, oracle.load(hd.S0, w.state_dtype))
+            assert d <= TOL[w.state_dtype], f"checkpoint of {(b, h)}: {d:.3e}"
+            for e in range(hd.count):
+                i = (hd.ckpt_pos + e) % w.L
+                assert np.array_equal(rk[s, h, i].view(np.uint8), hd.ek[e].view(np.uint8)), f"ring k {(b, h, e)}"
+                assert np.array_equal(rv[s, h, i].view(np.uint8), hd.ev[e].view(np.uint8)), f"ring v {(b, h, e)}"
+                assert rec[s, h, i, 0] == pytest.approx(hd.ea[e], rel=1e-5, abs=1e-30)
+                assert rec[s, h, i, 1] == pytest.approx(hd.eb[e], rel=1e-5, abs=1e-30)
+        assert int(self.err.item()) == 0
+
+
+@pytest.mark.parametrize("sdt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("L", [1, 4])
+def test_replay_steps_small_all_units(sdt, L):
+    w = wl.Workload("rs", B=3, Hk=1, Hv=2, dk=32, dv=32, steps=3 * L + 5, state_dtype=sdt, in_dtype="f32", L=L,
+                    seed=21)
+    H = Harness(w)
+    for t in range(w.steps):
+        H.window(wl.step_inputs(w, t), H.slots, 1, f"step {t}")
+    H.check_state()
+
+
+@pytest.mark.parametrize("sdt,idt", [("f32", "bf16"), ("bf16", "bf16"), ("f32", "f16")])
+def test_replay_multi_round_with_offsets(sdt, idt):
+    # 20 x 8 = 160 units over 152 persistent CTAs: a ragged second round
+    w = wl.Workload("rm", B=20, Hk=2, Hv=8, dk=128, dv=128, steps=24, state_dtype=sdt, in_dtype=idt, L=16,
+                    max_offset=15, seed=22)
+    H = Harness(w)
+    H.prefill(wl.start_offsets(w))
+    for t in range(w.steps):
+        H.window(wl.step_inputs(w, t), H.slots, 1, f"step {t}")
+    H.check_state()
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 48), (128, 256), (32, 96)])
+def test_replay_other_head_shapes(dk, dv):
+    w = wl.Workload("rh", B=5, Hk=2, Hv=4, dk=dk, dv=dv, steps=9, state_dtype="f32", in_dtype="bf16", L=4, seed=23)
+    H = Harness(w)
+    for t in range(w.steps):
+        H.window(wl.step_inputs(w, t), H.slots, 1, f"step {t}")
+    H.check_state()
+
+
+@pytest.mark.parametrize("T,L", [(2, 4), (3, 4), (4, 4), (4, 16), (8, 8), (5, 12)])
+@pytest.mark.parametrize("sdt", ["f32", "bf16"])
+def test_verify_and_rollback_small(T, L, sdt):
+    w = wl.Workload("vs", B=4, Hk=2, Hv=4, dk=64, dv=64, steps=10, state_dtype=sdt, in_dtype="bf16", L=L, T=T,
+                    seed=24)
+    H = Harness(w)
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, T, f"round {r}")
+        H.rollback(wl.accepted(w, r), T)
+        if r % 3 == 2:  # interleave plain replay steps
+            H.window(wl.step_inputs(w.with_(T=1), 500 + r), H.slots, 1, f"step after {r}")
+    H.check_state()
+
+
+@pytest.mark.parametrize("force", [True, False])
+def test_flush(force):
+    w = wl.Workload("fl", B=6, Hk=1, Hv=2, dk=128, dv=64, steps=1, state_dtype="bf16", in_dtype="bf16", L=8,
+                    max_offset=8, seed=25)
+    H = Harness(w)
+    H.prefill(wl.start_offsets(w))  # counts 0..8, some rings full
+    gdn.gdn_replay_flush(H.g.cache, torch.from_numpy(H.slots).cuda(), force, H.err)
+    for u in H.units:
+        H.heads[u].flush(force)
+    H.check_state()
+    H.window(wl.step_inputs(w, 0), H.slots, 1, "after flush")
+    H.check_state()
+
+
+def test_replay_ring_errors_are_reported_not_fatal():
+    w = wl.Workload("re", B=3, Hk=1, Hv=2, dk=32, dv=32, steps=1, state_dtype="f32", in_dtype="f32", L=4, seed=26)
+    H = Harness(w)
+    c = H.g.cache
+    c.pos[H.slots[1]] = 9  # count 9 > L
+    ck0 = c.ckpt.clone()
+    x = step_to_device(wl.step_inputs(w, 0), "f32")
+    out = torch.full((3, 1, 2, 32), 5.0, device="cuda")
+    gdn.gdn_replay_step(c, torch.from_numpy(H.slots).cuda(), x["q"], x["k"], x["v"], x["a"], x["b"], H.A_d, H.dt_d,
+                        out, H.err)
+    torch.cuda.synchronize()
+    assert int(H.err.item()) == gdn.DEVERR_RING
+    assert torch.all(out[1] == 0) and torch.all(out[0] != 5.0) and torch.all(out[2] != 5.0)
+    assert torch.equal(c.ckpt[H.slots[1]], ck0[H.slots[1]]) and int(c.pos[H.slots[1], 0]) == 9
+    # an accepted count outside [0, T-1] is refused without moving the pointer
+    err = dev_err()
+    acc = torch.tensor([0, 5, 1], dtype=torch.int32, device="cuda")
+    before = c.pos.clone()
+    gdn.gdn_rollback(c, torch.from_numpy(H.slots).cuda(), acc, 4, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & gdn.DEVERR_ACCEPT
+    assert torch.equal(c.pos[H.slots[1]], before[H.slots[1]])
+
+
+def _sampled(name: str, n_units: int):
+    w = wl.WORKLOADS[name]
+    units = sample_units(w.B, w.Hv, n_units, seed=5)
+    H = Harness(w, units)
+    if w.max_offset:
+        H.prefill(wl.start_offsets(w))
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, w.T, f"{name} round {r}")
+        if w.T > 1:
+            H.rollback(wl.accepted(w, r), w.T)
+    H.check_state()
+    return H.worst
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["replay_b256_f32", "replay_b256_bf16"])
+def test_replay_b256_sampled(name):
+    _sampled(name, 8)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["verify_b256_f32", "verify_b256_bf16"])
+def test_verify_b256_sampled(name):
+    _sampled(name, 8)
