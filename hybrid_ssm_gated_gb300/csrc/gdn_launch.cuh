@@ -7,6 +7,7 @@
 
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "gdn_decode.cuh"
@@ -39,21 +40,30 @@ inline cudaError_t device_info(DeviceInfo& out) {
     return cudaSuccess;
 }
 
-// Opt a kernel into `smem` bytes of dynamic shared memory (once per device and
-// size) and return how many CTAs of it fit on one SM.
+// Opt a kernel into the device's full dynamic shared memory (once per device
+// and kernel) and return how many CTAs using `smem` bytes fit on one SM.
 template <typename Kernel>
 cudaError_t prepare_kernel(Kernel kern, int threads, int smem, int& blocks_per_sm) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::map<std::tuple<int, const void*, int>, int> cache;
+    DeviceInfo di;
+    cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;
+    if (smem > di.smem_optin) return cudaErrorInvalidValue;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     std::lock_guard<std::mutex> g(mu);
-    auto key = std::make_pair(dev, smem);
+    const void* kp = reinterpret_cast<const void*>(kern);
+    const auto opted = std::make_tuple(dev, kp, -1);
+    if (cache.find(opted) == cache.end()) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin)) !=
+            cudaSuccess)
+            return e;
+        cache.emplace(opted, 0);
+    }
+    const auto key = std::make_tuple(dev, kp, smem);
     auto it = cache.find(key);
     if (it == cache.end()) {
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
-            return e;
         int bps = 0;
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, threads, smem)) != cudaSuccess) return e;
         if (bps < 1) return cudaErrorInvalidConfiguration;
