@@ -1,0 +1,510 @@
+"""Benchmark of the GDN recurrent-state decode step on GB300.
+
+Headline: GDN decode tokens/s at B=256, Hk=16, Hv=32, dk=dv=128 (bf16
+activations, fp32 state pool of 512 slots), and the decode kernel's achieved
+HBM bandwidth against the measured peak. One "step" is one decode step of the
+whole batch: gating, q/k normalisation, slot gather, fused update + readout,
+round + scatter -- all inside one kernel launch. The same JSON line also
+carries narrow-state decode, the ReplaySSM step and the T=4 verify window.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torch.distributed.run, one process per GPU, each with its
+own replica of the batch (the step has no cross-sequence exchange): weak
+scaling, barrier + synchronize around the timed region, max time over ranks.
+--impl reference times the CPU oracle (the plain fp64 C implementation) on
+the host cores for the same metric and workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode tokens/s at B=256,Hv=32,d=128; achieved HBM GB/s vs GB300 peak"
+B, HK, HV, DK, DV = 256, 16, 32, 128, 128
+NUM_SLOTS = 2 * B
+L_RING, T_VERIFY = 16, 4
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gdn_decode.cuh", "gdn_device.cuh", "gdn_launch.cuh"]
+
+
+# ------------------------------------------------------------------ bytes
+
+
+def decode_bytes_per_token(state_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+    """Algorithmic HBM bytes of one decode step of one sequence (all heads):
+    state read + write, q and k (per key head), v, a, b, output, slot index."""
+    return (2 * HV * DK * DV * state_bytes + 2 * HK * DK * in_bytes + HV * DV * in_bytes + 2 * HV * in_bytes +
+            HV * DV * out_bytes + 4)
+
+
+def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+    """Algorithmic bytes of one ReplaySSM call for one (sequence, value head):
+    checkpoint read, the `count` buffered ring entries read (raw k + the fp32
+    record {alpha, beta, w}), T tokens of inputs (q/k shared by Hv/Hk value
+    heads), T appended entries (raw k, raw v, record), T outputs, pointers,
+    and on a fold the checkpoint write."""
+    rec = (4 + DV) * 4
+    state = DK * DV * ckpt_bytes
+    inputs = T * (2 * DK * in_bytes * HK // HV + DV * in_bytes + 2 * in_bytes)
+    return (state + count * (DK * in_bytes + rec) + inputs + T * (DK * in_bytes + DV * in_bytes + rec) +
+            T * DV * out_bytes + 16 + (state if fold else 0))
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def load_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "hybrid_ssm_gated_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic() -> float | None:
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_b256_fp32state_traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except Exception:
+        return None
+    if doc.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return float(doc["dram_bytes_per_launch"])
+
+
+def pci_bus_id(dev: int) -> str | None:
+    for name in ("libcudart.so", "libcudart.so.13", "libcudart.so.12"):
+        try:
+            rt = ctypes.CDLL(name)
+            buf = ctypes.create_string_buffer(64)
+            if rt.cudaDeviceGetPCIBusId(buf, 64, dev) == 0:
+                return buf.value.decode()
+        except OSError:
+            continue
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.proc = None
+        self.target = None
+        bus = pci_bus_id(dev)
+        try:
+            rows = subprocess.run(["nvidia-smi", "--query-gpu=index,pci.bus_id", "--format=csv,noheader"],
+                                  capture_output=True, text=True, timeout=20).stdout.strip().splitlines()
+            for r in rows:
+                idx, b = [x.strip() for x in r.split(",")]
+                if bus and b.lower().endswith(bus.lower()[-12:]):
+                    self.target = idx
+            if self.target is None and len(rows) == 1:
+                self.target = rows[0].split(",")[0].strip()
+        except Exception:
+            self.target = None
+
+    def __enter__(self):
+        if self.target is not None:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=20)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def gpu_arm(args, rank: int, world: int) -> dict | None:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from hybrid_ssm_gated_gb300 import build, gdn
+    from hybrid_ssm_gated_gb300 import workload as wl
+
+    build.build()
+    gdn.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = wl.WORKLOADS["decode_b256_f32"].with_(seed=rank)
+    A_log, dt_bias = (torch.from_numpy(t).to(dev) for t in wl.head_params(w))
+    slots = torch.from_numpy(wl.slots(w)).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(1234 + rank)
+
+    def randn(*shape, dtype=torch.bfloat16, std=1.0):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(dtype)
+
+    q, k = randn(B, HK, DK), randn(B, HK, DK)
+    v, a, b = randn(B, HV, DV), randn(B, HV), randn(B, HV)
+    out = torch.empty(B, HV, DV, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def timed(fn, steps, warmup, per_launch=True):
+        """Run warmup, then `steps` timed calls; returns (elapsed ms over ranks, mean launch ms)."""
+        for _ in range(warmup):
+            fn()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+            if per_launch else []
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            if per_launch:
+                evs[i][0].record(stream)
+            fn()
+            if per_launch:
+                evs[i][1].record(stream)
+        t1.record(stream)
+        barrier()
+        elapsed = t0.elapsed_time(t1)
+        launch = statistics.fmean(s.elapsed_time(e) for s, e in evs) if per_launch else elapsed / steps
+        return max_over_ranks(elapsed), launch
+
+    peak, peak_kind = load_peaks()
+    result = {}
+
+    # -------- headline: decode, fp32 state pool
+    pool = (torch.randn(NUM_SLOTS, HV, DV, DK, generator=gen, device=dev) * 0.1).float()
+    step = lambda: gdn.gdn_decode_step(pool, slots, q, k, v, a, b, A_log, dt_bias, out, err, stream)
+    sampler = ClockSampler(dev.index)
+    for _ in range(args.warmup):
+        step()
+    with sampler:
+        elapsed, launch_ms = timed(step, args.steps, 0)
+    clocks = sampler.summary()
+    bpt = decode_bytes_per_token(4)
+    tok_s = world * B * args.steps / (elapsed / 1e3)
+    achieved = bpt * B / (launch_ms / 1e3) / 1e9
+    result.update({
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "gdn_decode_b256_fp32_state", "B": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                   "state_dtype": "fp32", "in_dtype": "bf16", "out_dtype": "fp32", "num_slots": NUM_SLOTS,
+                   "slots": "seeded permutation", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 512 MiB of state read+written per step (L2 129 MB)"},
+        "hbm_gbs": achieved,
+        "bytes_per_token": bpt,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(), "peak_kind": peak_kind,
+                     "kernel": "gdn::decode_kernel<float,128,8,8,4>", "launch_us": launch_ms * 1e3,
+                     "algorithmic_bytes_per_launch": bpt * B},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    })
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during the headline run")
+
+    # -------- e2e through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, ha, hb, hs = pin(q), pin(k), pin(v), pin(a), pin(b), pin(slots)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk_, dv_, da, db, ds = (torch.empty_like(t) for t in (q, k, v, a, b, slots))
+
+    def e2e_step():
+        for d, h in ((dq, hq), (dk_, hk), (dv_, hv), (da, ha), (db, hb), (ds, hs)):
+            d.copy_(h, non_blocking=True)
+        gdn.gdn_decode_step(pool, ds, dq, dk_, dv_, da, db, A_log, dt_bias, out, err, stream)
+        hout.copy_(out, non_blocking=True)
+
+    e2e_steps = max(10, args.steps // 4)
+    e_elapsed, _ = timed(e2e_step, e2e_steps, max(3, args.warmup // 4), per_launch=False)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb, hs))
+    result["e2e"] = {"value": world * B * e2e_steps / (e_elapsed / 1e3), "unit": "tokens/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+                     "steps": e2e_steps, "ms_per_step": e_elapsed / e2e_steps}
+    result["gpu_launches"] += e2e_steps
+    del pool
+
+    # -------- other modes (same JSON line)
+    modes = {}
+    msteps = max(20, args.steps // 10)
+    for name, sdt, ss in (("decode_bf16_state", torch.bfloat16, 2), ("decode_fp16_state", torch.float16, 2)):
+        p = (torch.randn(NUM_SLOTS, HV, DV, DK, generator=gen, device=dev) * 0.1).to(sdt)
+        el, lm = timed(lambda: gdn.gdn_decode_step(p, slots, q, k, v, a, b, A_log, dt_bias, out, err, stream),
+                       msteps, args.warmup)
+        bt = decode_bytes_per_token(ss)
+        gbs = bt * B / (lm / 1e3) / 1e9
+        modes[name] = {"tokens_per_s": world * B * msteps / (el / 1e3), "us_per_step": el / msteps * 1e3,
+                       "hbm_gbs": gbs, "frac": gbs / peak, "bytes_per_token": bt}
+        result["gpu_launches"] += msteps
+        del p
+
+    offsets = wl.start_offsets(wl.WORKLOADS["replay_b256_f32"])
+    slot_np = wl.slots(w)
+    for ckname, cdt, cs in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        cache = gdn.ReplayCache.allocate(NUM_SLOTS, HV, DK, DV, L_RING, cdt, torch.bfloat16, device=dev)
+        cache.ckpt.normal_(0, 0.1, generator=gen)
+        counts = np.zeros(NUM_SLOTS, dtype=np.int64)
+        counts[slot_np] = offsets
+        cache.pos.copy_(torch.from_numpy(np.repeat(counts[:, None], HV, 1).astype(np.int32)))
+        # warm the ring so buffered entries hold real data: run L steps first
+        out1 = torch.empty(B, 1, HV, DV, device=dev)
+        rstep = lambda: gdn.gdn_replay_step(cache, slots, q, k, v, a, b, A_log, dt_bias, out1, err, stream)
+        for _ in range(L_RING):
+            rstep()
+        torch.cuda.synchronize()
+        c = (cache.pos - cache.ckpt_pos)[slots.long(), 0].cpu().numpy().astype(np.int64)
+        rsteps = max(32, (args.steps // 20) // L_RING * L_RING)
+        total_bytes = 0
+        cc = c.copy()
+        for _ in range(rsteps):  # host replay of the ring counts: fold when an append would overflow
+            fold = cc + 1 > L_RING
+            total_bytes += HV * sum(replay_unit_bytes(int(x), 1, bool(f), cs) for x, f in zip(cc, fold))
+            cc = np.where(fold, 0, cc) + 1
+        el, lm = timed(rstep, rsteps, 3)
+        gbs = total_bytes / rsteps / (lm / 1e3) / 1e9
+        modes[f"replay_step_{ckname}_ckpt"] = {
+            "tokens_per_s": world * B * rsteps / (el / 1e3), "us_per_step": el / rsteps * 1e3, "hbm_gbs": gbs,
+            "frac": gbs / peak, "bytes_per_token": total_bytes / rsteps / B, "L": L_RING,
+            "start_offsets": "uniform in [0, 15]",
+            "state_write_bytes_per_token": HV * DK * DV * cs / L_RING}
+        result["gpu_launches"] += rsteps
+
+        # verify T=4 + rollback, accepted uniform in {0..3}
+        T = T_VERIFY
+        q4, k4 = randn(B, T, HK, DK), randn(B, T, HK, DK)
+        v4, a4, b4 = randn(B, T, HV, DV), randn(B, T, HV), randn(B, T, HV)
+        out4 = torch.empty(B, T, HV, DV, device=dev)
+        acc = torch.randint(0, T, (B,), generator=gen, device=dev, dtype=torch.int32)
+
+        def vround():
+            gdn.gdn_verify_window(cache, slots, q4, k4, v4, a4, b4, A_log, dt_bias, out4, err, stream)
+            gdn.gdn_rollback(cache, slots, acc, T, err, stream)
+
+        vrounds = max(16, args.steps // 40)
+        el, lm = timed(vround, vrounds, 3)
+        accepted_tokens = float((acc.float() + 1).sum().item())
+        modes[f"verify_T4_{ckname}_ckpt"] = {
+            "window_tokens_per_s": world * B * T * vrounds / (el / 1e3),
+            "accepted_tokens_per_s": world * accepted_tokens * vrounds / (el / 1e3),
+            "us_per_round": el / vrounds * 1e3, "T": T, "L": L_RING}
+        result["gpu_launches"] += 2 * vrounds
+        del cache
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during the mode runs")
+    result["modes"] = modes
+    return result
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_decode_rate(seconds: float = 2.0, sample_seqs: int = 32) -> dict:
+    """Time the CPU oracle on a bounded sample of the headline workload:
+    `sample_seqs` sequences x all 32 heads per step, steps repeated until
+    `seconds` of wall time, all host cores."""
+    import numpy as np
+
+    import oracle
+    from hybrid_ssm_gated_gb300 import workload as wl
+
+    w = wl.WORKLOADS["decode_b256_f32"].with_(B=sample_seqs, num_slots=sample_seqs, slot_mode="identity")
+    pool = np.stack([wl.slot_state(w, s) for s in range(sample_seqs)])
+    A_log, dt_bias = wl.head_params(w)
+    slots = wl.slots(w)
+    cores = os.cpu_count() or 1
+    run = lambda x: oracle.decode_step(pool, "f32", slots, x["q"], x["k"], x["v"], x["a"], x["b"], "bf16", A_log,
+                                       dt_bias, nthreads=cores)
+    x0 = wl.step_inputs(w, 0)
+    ts = time.perf_counter()
+    run(x0)  # calibration step
+    steps = int(min(50, max(1, seconds / max(time.perf_counter() - ts, 1e-6))))
+    xs = [wl.step_inputs(w, s) for s in range(1, steps + 1)]
+    ts = time.perf_counter()
+    for x in xs:
+        run(x)
+    el = time.perf_counter() - ts
+    return {"value": sample_seqs * steps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{sample_seqs} sequences x {HV} heads x {steps} decode steps of the B=256 workload "
+                      f"(fp32 state, bf16 inputs), fp64 C oracle, OpenMP over (sequence, head)",
+            "seconds": el}
+
+
+def reference_arm(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    samples = max(1, min(args.steps, 5))
+    oracle_decode_rate(seconds=0.2)  # untimed warm-up (builds the oracle, pages in libraries)
+    rates = [oracle_decode_rate(seconds=1.0) for _ in range(samples)]
+    v = statistics.median(r["value"] for r in rates)
+    cb = dict(rates[0])
+    cb["value"] = v
+    cb["sample"] += f"; median of {samples} samples"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": samples, "warmup": 1, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "gdn_decode_b256_fp32_state", "B": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                       "state_dtype": "fp32", "in_dtype": "bf16"},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ profiling cases
+
+
+def run_case(args) -> None:
+    """Run a few untimed launches of one kernel for a profiler (no JSON line).
+
+    decode:  B sequences, fp32/bf16/fp16 state pool of 2B slots.
+    replay:  ReplaySSM steps, L=16 ring pre-filled to start offsets in [0, 15].
+    verify:  T=4 verify windows + rollbacks on the same cache.
+    """
+    import numpy as np
+    import torch
+
+    from hybrid_ssm_gated_gb300 import build, gdn
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    Bc = args.B
+    sdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.state_dtype]
+    rnd = lambda *s: torch.randn(*s, generator=g, device=dev).to(torch.bfloat16)
+    A_log = torch.rand(HV, generator=g, device=dev) * 2
+    dt_bias = torch.rand(HV, generator=g, device=dev) * 2 - 1
+    slots = torch.randperm(2 * Bc, generator=g, device=dev)[:Bc].to(torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.case == "decode":
+        pool = (torch.randn(2 * Bc, HV, DV, DK, generator=g, device=dev) * 0.1).to(sdt)
+        q, k, v, a, b = rnd(Bc, HK, DK), rnd(Bc, HK, DK), rnd(Bc, HV, DV), rnd(Bc, HV), rnd(Bc, HV)
+        out = torch.empty(Bc, HV, DV, device=dev)
+        for _ in range(args.steps):
+            gdn.gdn_decode_step(pool, slots, q, k, v, a, b, A_log, dt_bias, out, err)
+    else:
+        T = T_VERIFY if args.case == "verify" else 1
+        cache = gdn.ReplayCache.allocate(2 * Bc, HV, DK, DV, L_RING, sdt, torch.bfloat16, device=dev)
+        cache.ckpt.normal_(0, 0.1, generator=g)
+        off = torch.randint(0, L_RING, (2 * Bc, 1), generator=g, device=dev).to(torch.int32)
+        cache.pos.copy_(off.expand(2 * Bc, HV))
+        q, k, v, a, b = rnd(Bc, T, HK, DK), rnd(Bc, T, HK, DK), rnd(Bc, T, HV, DV), rnd(Bc, T, HV), rnd(Bc, T, HV)
+        out = torch.empty(Bc, T, HV, DV, device=dev)
+        acc = torch.randint(0, T, (Bc,), generator=g, device=dev, dtype=torch.int32)
+        for _ in range(args.steps):
+            if T == 1:
+                gdn.gdn_replay_step(cache, slots, q, k, v, a, b, A_log, dt_bias, out, err)
+            else:
+                gdn.gdn_verify_window(cache, slots, q, k, v, a, b, A_log, dt_bias, out, err)
+                gdn.gdn_rollback(cache, slots, acc, T, err)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error word {int(err.item())}")
+    print(f"case {args.case} ok")
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["decode", "replay", "verify"],
+                    help="run --steps untimed launches of one kernel for a profiler and exit")
+    ap.add_argument("--B", type=int, default=B, help="batch of --case")
+    ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16", "f16"], help="state dtype of --case")
+    args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = gpu_arm(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = oracle_decode_rate()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
