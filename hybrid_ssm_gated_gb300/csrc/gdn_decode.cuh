@@ -126,41 +126,54 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                 const int s_i = __shfl_sync(FULL_MASK, slot, i);
                 const float al = __shfl_sync(FULL_MASK, alpha, i);
                 const float be = __shfl_sync(FULL_MASK, beta, i);
+                // A single thread issues a bulk copy only every ~0.25 us, so the unit's
+                // copies are spread over lanes: lanes 0-2 the q/k/v rows, lane c chunk c.
+                const int hs = n % NH;
+                unsigned char* head = heads + hs * C::HEAD;
                 if (lane == 0) {
-                    const int hs = n % NH;
                     if (n >= NH) ok = mbar_wait(&hempty[hs], ((n / NH) + 1) & 1);
                     if (ok) {
-                        unsigned char* head = heads + hs * C::HEAD;
                         reinterpret_cast<int*>(head)[0] = s_i;
                         reinterpret_cast<float*>(head)[1] = al;
                         reinterpret_cast<float*>(head)[2] = be;
-                        if (s_i >= 0) {
-                            const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
+                        if (s_i >= 0)
                             mbar_arrive_expect_tx(&hfull[hs], 2 * qbytes + vbytes);
-                            const int64_t qrow = (int64_t)b * p.Hk + kh;
-                            bulk_load(head + C::OFF_Q, static_cast<const char*>(p.q) + qrow * qbytes, qbytes,
-                                      &hfull[hs]);
-                            bulk_load(head + C::OFF_K, static_cast<const char*>(p.k) + qrow * qbytes, qbytes,
-                                      &hfull[hs]);
-                            bulk_load(head + C::OFF_V, static_cast<const char*>(p.v) + (int64_t)unit * vbytes,
-                                      vbytes, &hfull[hs]);
-                            const char* src = static_cast<const char*>(p.pool) +
-                                              ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES;
-                            for (int c = 0; c < p.nchunk; ++c, ++m) {
-                                const int cs = m % NS;
-                                if (m >= NS && !(ok = mbar_wait(&cempty[cs], ((m / NS) + 1) & 1))) break;
-                                mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src + (int64_t)c * cbytes, cbytes,
-                                               &cfull[cs], pol);
-                            }
-                        } else {
+                        else
                             mbar_arrive(&hfull[hs]);
-                        }
                         ++nh;
                     }
                 }
                 ok = __shfl_sync(FULL_MASK, ok, 0);
                 if (!ok) break;
+                if (s_i >= 0) {
+                    const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
+                    const int64_t qrow = (int64_t)b * p.Hk + kh;
+                    if (lane == 0)
+                        bulk_load(head + C::OFF_Q, static_cast<const char*>(p.q) + qrow * qbytes, qbytes, &hfull[hs]);
+                    else if (lane == 1)
+                        bulk_load(head + C::OFF_K, static_cast<const char*>(p.k) + qrow * qbytes, qbytes, &hfull[hs]);
+                    else if (lane == 2)
+                        bulk_load(head + C::OFF_V, static_cast<const char*>(p.v) + (int64_t)unit * vbytes, vbytes,
+                                  &hfull[hs]);
+                    if (lane < p.nchunk) {
+                        const uint32_t mc = m + lane;
+                        const int cs = mc % NS;
+                        bool lok = mc < NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
+                        if (lok) {
+                            const char* src = static_cast<const char*>(p.pool) +
+                                              ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)lane * cbytes;
+                            mbar_arrive_expect_tx(&cfull[cs], cbytes);
+                            bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                        }
+                        ok = lok;
+                    }
+                    ok = __all_sync(FULL_MASK, ok);
+                    if (!ok) {
+                        m += __popc(__ballot_sync(FULL_MASK, lane < p.nchunk && ok));
+                        break;
+                    }
+                    m += p.nchunk;
+                }
             }
         }
         if (!ok && lane == 0) {
@@ -212,6 +225,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
 #pragma unroll
             for (int e = 0; e < C::E; ++e) kn[e] *= ik, qn[e] *= iq, qk = fmaf(kn[e], qn[e], qk);
             qk = group_sum<C::LPR>(qk);
+            // packed FP32x2 operands: two state elements per instruction
+            float2 kn2[C::E / 2], qn2[C::E / 2];
+#pragma unroll
+            for (int e = 0; e < C::E / 2; ++e)
+                kn2[e] = make_float2(kn[2 * e], kn[2 * e + 1]), qn2[e] = make_float2(qn[2 * e], qn[2 * e + 1]);
 
             const int b = unit / p.Hv, h = unit - b * p.Hv;
             char* gstate = static_cast<char*>(p.pool) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
@@ -222,7 +240,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     return;
                 }
                 const unsigned char* tile = chunks + cs * CHUNK_BYTES;
-                for (int ps = cw; ps < passes; ps += NCW) {
+                // the unit's warp passes are spread over the consumer warps across chunks
+                for (int ps = ((cw - c * passes) % NCW + NCW) % NCW; ps < passes; ps += NCW) {
                     const int r = ps * C::RPP + rsub;
                     const int j = c * p.rows + r;
                     float s[C::E];
@@ -232,15 +251,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                                                                           (cc * C::LPR + pg) * 16);
                         Store<ST>::unpack(raw, s + cc * C::VEC);
                     }
-                    float u = 0.f, pq = 0.f;
+                    float2 u2 = make_float2(0.f, 0.f), p2 = u2;
 #pragma unroll
-                    for (int e = 0; e < C::E; ++e) u = fmaf(s[e], kn[e], u), pq = fmaf(s[e], qn[e], pq);
-                    u = group_sum<C::LPR>(u);
-                    pq = group_sum<C::LPR>(pq);
+                    for (int e = 0; e < C::E / 2; ++e) {
+                        const float2 s2 = make_float2(s[2 * e], s[2 * e + 1]);
+                        u2 = __ffma2_rn(s2, kn2[e], u2);
+                        p2 = __ffma2_rn(s2, qn2[e], p2);
+                    }
+                    const float u = group_sum<C::LPR>(u2.x + u2.y);
+                    const float pq = group_sum<C::LPR>(p2.x + p2.y);
                     const float vj = load_elem(head + C::OFF_V, j, p.in_dtype);
                     const float delta = beta * (vj - alpha * u);
+                    const float2 al2 = make_float2(alpha, alpha), d2 = make_float2(delta, delta);
 #pragma unroll
-                    for (int e = 0; e < C::E; ++e) s[e] = fmaf(kn[e], delta, alpha * s[e]);
+                    for (int e = 0; e < C::E / 2; ++e) {
+                        const float2 r2 = __ffma2_rn(kn2[e], d2, __fmul2_rn(make_float2(s[2 * e], s[2 * e + 1]), al2));
+                        s[2 * e] = r2.x, s[2 * e + 1] = r2.y;
+                    }
                     char* dst = gstate + (int64_t)j * C::ROW_BYTES;
 #pragma unroll
                     for (int cc = 0; cc < C::NC; ++cc)

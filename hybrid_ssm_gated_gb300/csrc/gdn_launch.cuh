@@ -73,8 +73,17 @@ cudaError_t prepare_kernel(Kernel kern, int threads, int smem, int& blocks_per_s
     return cudaSuccess;
 }
 
-// Decode: 8 consumer warps, 8 chunk stages of 16 KB, 4 head stages.
-constexpr int DEC_NCW = 8, DEC_NS = 8, DEC_NH = 4;
+// Decode: consumer warps, 16 KB chunk stages and head stages per CTA.
+#ifndef GDN_DECODE_CONSUMER_WARPS
+#define GDN_DECODE_CONSUMER_WARPS 16
+#endif
+#ifndef GDN_DECODE_CHUNK_STAGES
+#define GDN_DECODE_CHUNK_STAGES 6
+#endif
+#ifndef GDN_DECODE_HEAD_STAGES
+#define GDN_DECODE_HEAD_STAGES 4
+#endif
+constexpr int DEC_NCW = GDN_DECODE_CONSUMER_WARPS, DEC_NS = GDN_DECODE_CHUNK_STAGES, DEC_NH = GDN_DECODE_HEAD_STAGES;
 
 template <typename ST, int DK>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -91,12 +100,18 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Replay: 8 consumer warps; chunk stages as many as fit (2..6).
-constexpr int REP_NCW = 8, REP_NS_MAX = 6;
+// Replay: prep warps and row warps beside the two producer warps.
+#ifndef GDN_REPLAY_PREP_WARPS
+#define GDN_REPLAY_PREP_WARPS 2
+#endif
+#ifndef GDN_REPLAY_ROW_WARPS
+#define GDN_REPLAY_ROW_WARPS 8
+#endif
+constexpr int REP_NPW = GDN_REPLAY_PREP_WARPS, REP_NRW = GDN_REPLAY_ROW_WARPS;
 
-// Fill the shared-memory layout fields of `a` (needs dk, T, L, dv, in_dtype).
+// Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype).
 // Returns the total dynamic shared memory in bytes, or -1 if it cannot fit.
-template <int DK, int TMAX>
+template <int DK, int TMAX, int NPW>
 int replay_layout(ReplayArgs& a, int smem_limit) {
     const int in_sz = dtype_size(a.in_dtype);
     const int T = a.T, L = a.L;
@@ -106,31 +121,38 @@ int replay_layout(ReplayArgs& a, int smem_limit) {
     a.off_rk = align_up(a.off_wv + T * a.dv * in_sz, 16);
     a.off_rec = a.off_rk + L * DK * in_sz;
     a.head_bytes = align_up(a.off_rec + L * (4 + a.dv) * 4, 128);
-    a.off_khat = 0;
-    a.off_qhat = (L + TMAX) * DK * 4;
-    a.off_coef = a.off_qhat + TMAX * DK * 4;
+    a.off_kw = 0;
+    a.off_qw = TMAX * DK * 4;
+    a.off_khat = 2 * TMAX * DK * 4;
+    a.off_coef = a.off_khat + L * DK * 4;
     const int coef_floats = 2 * TMAX * (L + TMAX) + 2 * TMAX + 1 + L;
     a.scratch_bytes = align_up(a.off_coef + coef_floats * 4, 128);
-    const int fixed = REPLAY_NH * a.head_bytes + 2 * a.scratch_bytes;
-    int ns = REP_NS_MAX;
-    auto total = [&](int n) { return n * CHUNK_BYTES + fixed + (2 * n + 2 * REPLAY_NH + 2) * 8; };
-    while (ns >= 2 && total(ns) > smem_limit) --ns;
-    if (ns < 2) return -1;
-    a.nstage = ns;
+    a.nscr = NPW + 1;
+    auto total = [&](int ns, int nh) {
+        return ns * CHUNK_BYTES + nh * a.head_bytes + a.nscr * a.scratch_bytes + (2 * ns + 2 * nh + 2 * a.nscr) * 8;
+    };
+    // deepest head ring first (prep lookahead), then chunk stages; at least 3 chunk stages if possible
+    int ns = 0, nh = 0;
+    for (int min_ns = 3; min_ns >= 2 && !ns; --min_ns)
+        for (int h = NPW + 3; h >= 2 && !ns; --h)
+            if (total(min_ns, h) <= smem_limit) ns = min_ns, nh = h;
+    if (!ns) return -1;
+    while (ns < 6 && total(ns + 1, nh) <= smem_limit) ++ns;
+    a.nstage = ns, a.nhead = nh;
     a.heads_off = ns * CHUNK_BYTES;
-    a.scratch_off = a.heads_off + REPLAY_NH * a.head_bytes;
-    a.bars_off = a.scratch_off + 2 * a.scratch_bytes;
-    return total(ns);
+    a.scratch_off = a.heads_off + nh * a.head_bytes;
+    a.bars_off = a.scratch_off + a.nscr * a.scratch_bytes;
+    return total(ns, nh);
 }
 
 template <typename ST, int DK, int TMAX>
 cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
-    using C = ReplayCfg<ST, DK, TMAX, REP_NCW>;
-    auto kern = replay_kernel<ST, DK, TMAX, REP_NCW>;
+    using C = ReplayCfg<ST, DK, TMAX, REP_NPW, REP_NRW>;
+    auto kern = replay_kernel<ST, DK, TMAX, REP_NPW, REP_NRW>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;
-    const int smem = replay_layout<DK, TMAX>(a, di.smem_optin);
+    const int smem = replay_layout<DK, TMAX, REP_NPW>(a, di.smem_optin);
     too_big = smem < 0;
     if (too_big) return cudaSuccess;
     int bps = 0;

@@ -15,7 +15,8 @@ import re
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libgdn.so")
+# GDN_LIBRARY may point at another build of the same library (e.g. a tuning variant)
+LIB_PATH = os.environ.get("GDN_LIBRARY") or os.path.join(HERE, "lib", "libgdn.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "gdn.h")
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
