@@ -91,6 +91,7 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
     if (!dtype_ok(c->ckpt_dtype) || !dtype_ok(c->ring_dtype))
         return fail(GDN_ERR_DTYPE, "%s: unsupported cache dtype (ckpt=%d ring=%d)", fn, c->ckpt_dtype, c->ring_dtype);
     if (c->L < 1 || c->L > gdn::L_MAX) return fail(GDN_ERR_WINDOW, "%s: L=%d not in [1, 32]", fn, c->L);
+    if (dims->dv % 32 != 0) return fail(GDN_ERR_SHAPE, "%s: dv=%d must be a multiple of 32", fn, dims->dv);
     if (T > 0) {
         if (T > c->L || T > gdn::WINDOW_MAX)
             return fail(GDN_ERR_WINDOW, "%s: window T=%d exceeds min(L=%d, 8)", fn, T, c->L);

@@ -155,24 +155,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     else if (lane == 2)
                         bulk_load(head + C::OFF_V, static_cast<const char*>(p.v) + (int64_t)unit * vbytes, vbytes,
                                   &hfull[hs]);
-                    if (lane < p.nchunk) {
-                        const uint32_t mc = m + lane;
-                        const int cs = mc % NS;
-                        bool lok = mc < NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
-                        if (lok) {
-                            const char* src = static_cast<const char*>(p.pool) +
-                                              ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)lane * cbytes;
-                            mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                            bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                    // at most NS lanes at a time, so no lane waits for a stage another lane is about to fill
+                    for (int c0 = 0; c0 < p.nchunk && ok; c0 += NS) {
+                        const int c = c0 + lane;
+                        if (lane < NS && c < p.nchunk) {
+                            const uint32_t mc = m + c;
+                            const int cs = mc % NS;
+                            ok = mc < NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
+                            if (ok) {
+                                const char* src = static_cast<const char*>(p.pool) +
+                                                  ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)c * cbytes;
+                                mbar_arrive_expect_tx(&cfull[cs], cbytes);
+                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                            }
                         }
-                        ok = lok;
-                    }
-                    ok = __all_sync(FULL_MASK, ok);
-                    if (!ok) {
-                        m += __popc(__ballot_sync(FULL_MASK, lane < p.nchunk && ok));
-                        break;
+                        ok = __all_sync(FULL_MASK, ok);
                     }
                     m += p.nchunk;
+                    if (!ok) break;
                 }
             }
         }

@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
+// Wait until a shared-memory tag holds `want` (a message published with a
+// fence before the tag store); false after WAIT_LIMIT_NS. Tags carry unit or
+// chunk numbers that are never reused within a launch, so unlike an mbarrier
+// parity wait a slow waiter cannot mistake an older round for its own.
+__device__ __forceinline__ bool wait_tag(const volatile int* tag, int want) {
+    if (*tag == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (*tag != want) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+    return true;
+}
+
 // L2 policy for data read once (state tiles): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -123,21 +123,23 @@ int replay_layout(ReplayArgs& a, int smem_limit) {
     a.head_bytes = align_up(a.off_rec + L * (4 + a.dv) * 4, 128);
     a.off_kw = 0;
     a.off_qw = TMAX * DK * 4;
-    a.off_khat = 2 * TMAX * DK * 4;
-    a.off_coef = a.off_khat + L * DK * 4;
+    a.off_coef = 2 * TMAX * DK * 4;
     const int coef_floats = 2 * TMAX * (L + TMAX) + 2 * TMAX + 1 + L;
     a.scratch_bytes = align_up(a.off_coef + coef_floats * 4, 128);
-    a.nscr = NPW + 1;
+    // scratch slot s serves units n = s mod nscr, all prepared by warp s mod NPW
+    a.nscr = 2 * NPW;
     auto total = [&](int ns, int nh) {
-        return ns * CHUNK_BYTES + nh * a.head_bytes + a.nscr * a.scratch_bytes + (2 * ns + 2 * nh + 2 * a.nscr) * 8;
+        // mbarriers: 2 per chunk and head stage, 1 per scratch slot; tags: 16 B per chunk stage, 4 B per slot
+        return ns * CHUNK_BYTES + nh * a.head_bytes + a.nscr * a.scratch_bytes + (2 * ns + 2 * nh + a.nscr) * 8 +
+               ns * 16 + align_up((a.nscr + nh) * 4, 16);
     };
-    // deepest head ring first (prep lookahead), then chunk stages; at least 3 chunk stages if possible
+    // deepest head ring first (prep lookahead, at least NPW), then chunk stages
     int ns = 0, nh = 0;
-    for (int min_ns = 3; min_ns >= 2 && !ns; --min_ns)
-        for (int h = NPW + 3; h >= 2 && !ns; --h)
+    for (int min_ns = 4; min_ns >= 2 && !ns; --min_ns)
+        for (int h = NPW + 3; h >= NPW && h >= 2 && !ns; --h)
             if (total(min_ns, h) <= smem_limit) ns = min_ns, nh = h;
     if (!ns) return -1;
-    while (ns < 6 && total(ns + 1, nh) <= smem_limit) ++ns;
+    while (ns < 12 && total(ns + 1, nh) <= smem_limit) ++ns;
     a.nstage = ns, a.nhead = nh;
     a.heads_off = ns * CHUNK_BYTES;
     a.scratch_off = a.heads_off + nh * a.head_bytes;

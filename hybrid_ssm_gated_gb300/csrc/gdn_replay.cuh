@@ -17,25 +17,38 @@
 //   S_{e-1}^T k_e = G(e-1) S0^T k_e + sum_{f<e}  A(f,e-1) (k_f.k_e) w_f
 //   w_e           = beta_e (v_e - alpha_e S_{e-1}^T k_e)
 //   o_e = S_e^T q = G(e)   S0^T q   + sum_{f<=e} A(f,e)   (k_f.q)   w_f
-// The ring keeps w_f (fp32) beside each entry's raw inputs, so one pass over
-// S0 -- two dot products per state element per window token -- and O(count)
-// vector work give every output; S_t itself is only materialised (in FP32
-// registers) when the ring is folded: S0 <- round(G S0 + sum A k w^T).
+// The ring keeps w_f (fp32) and the key's inverse norm beside each entry's raw
+// inputs, so one pass over S0 -- two dot products per state element per
+// window token -- and O(count) vector work give every output; S_t itself is
+// only materialised (in FP32 registers) when the ring is folded:
+// S0 <- round(G S0 + sum A k w^T).
 //
-// Kernel shape: persistent CTAs over (sequence, value head) units with four
-// warp roles, so the per-unit scalar work never stalls the state stream:
-//   warp 0       head producer: per-unit metadata (slot, pointers, gates)
-//                for 32 units at a time, then bulk copies (TMA engine) of the
-//                unit's window rows and buffered ring entries into a head ring;
-//   warp 1       chunk producer: streams S0 in 16 KB chunks into a chunk ring;
-//   NPW warps    prep: one warp prepares one whole unit -- normalised window
-//                keys/queries, key-key / key-query dot products times decay
-//                products (the coefficients above), fold coefficients -- into
-//                a scratch slot, appends the window to the ring and moves the
-//                pointers;
-//   NRW warps    rows: stream S0 rows from the chunk ring, fold if required,
-//                two dot products per element per window token, the w
-//                recursion, and the outputs.
+// Kernel shape: persistent CTAs over (sequence, value head) units, four warp
+// roles, so the per-unit scalar work never stalls the state stream:
+//   warp 0       head producer: per-unit metadata (slot, pointers, gates) for
+//                32 units at a time, then the unit's window rows and buffered
+//                ring entries into a head ring (bulk copies, one per lane);
+//   warp 1       chunk producer: streams S0 in 16 KB chunks into a chunk ring
+//                (lane c issues chunk c of a unit) and tags each stage with
+//                its unit; after the last chunk it posts one stop tag per row
+//                warp;
+//   NPW warps    prep: one warp prepares one whole unit into a scratch slot --
+//                normalised window keys/queries, one lane per buffered entry
+//                for its dot products with the window, decay products by a
+//                suffix-product scan across lanes -- then appends the window
+//                to the ring and moves the pointers;
+//   NRW warps    rows: each takes whole chunks, round robin. Window size 1:
+//                eight row passes of partial dot products, then one
+//                reduce-scatter across the row's lanes leaves every lane
+//                owning one row, so the w recursion, output and w store run
+//                once per row, coalesced. Larger windows reduce per pass.
+// Hand-offs: an mbarrier parity wait cannot tell a phase from the one two
+// rounds earlier, so it is used alone only where the waiter sees every phase
+// of that barrier in order (the producers; prep warps on their own scratch
+// slots, the scratch ring depth being a multiple of the prep-warp count).
+// Elsewhere the filler first publishes a unit / chunk number tag and the
+// waiter checks the tag before the barrier (prep warps and head stages; row
+// warps, which take every NRW-th chunk, and chunk stages / scratch slots).
 // Every wait is bounded (GDN_DEVERR_TIMEOUT, then return).
 #pragma once
 
@@ -73,7 +86,7 @@ struct ReplayArgs {
     // shared-memory layout, bytes
     int head_bytes, off_wq, off_wk, off_wv, off_rk, off_rec;  // inside a head stage
     int heads_off, scratch_off, scratch_bytes, bars_off;      // inside the CTA's buffer
-    int off_kw, off_qw, off_khat, off_coef;                   // inside a scratch slot
+    int off_kw, off_qw, off_coef;                             // inside a scratch slot
 };
 
 constexpr int REPLAY_META = 128;  // bytes of per-unit metadata at the start of a head stage
@@ -83,12 +96,12 @@ struct ReplayCfg {
     static constexpr int VEC = Store<ST>::VEC;
     static constexpr int E = TMAX <= 2 ? 16 : 8;  // state elements per lane per row
     static constexpr int NC = E / VEC;
-    static constexpr int LPR = DK / E;
+    static constexpr int LPR = DK / E;    // lanes per row
     static constexpr int RPP = 32 / LPR;  // rows per warp pass
     static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
-    static constexpr int PE = DK / 32;  // elements per lane when one warp handles a vector
     static constexpr int THREADS = (2 + NPW + NRW) * 32;
     static constexpr bool KW_REG = TMAX <= 4;  // window vectors held in registers by the row warps
+    static constexpr bool FAST = TMAX == 1;    // one row per lane after a reduce-scatter
     static_assert(E % VEC == 0 && DK % E == 0 && LPR <= 32 && DK % 32 == 0, "unsupported dk");
 };
 
@@ -107,6 +120,27 @@ static_assert(sizeof(ReplayMeta) <= REPLAY_META, "meta too large");
 
 __device__ __forceinline__ float warp_sum(float x) { return group_sum<32>(x); }
 
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(n) : "memory");
+}
+
+// Reduce-scatter of x[0..G) over aligned groups of G lanes: afterwards lane
+// (group position g) holds the group total of x[g]. G lanes, G values.
+template <int G>
+__device__ __forceinline__ float reduce_scatter(float (&x)[G], int g) {
+#pragma unroll
+    for (int half = G / 2; half >= 1; half >>= 1) {
+        const bool upper = (g & half) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? x[i] : x[i + half];
+            const float keep = upper ? x[i + half] : x[i];
+            x[i] = keep + __shfl_xor_sync(FULL_MASK, send, half);
+        }
+    }
+    return x[0];
+}
+
 template <typename ST, int DK, int TMAX, int NPW, int NRW>
 __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const ReplayArgs p) {
     using C = ReplayCfg<ST, DK, TMAX, NPW, NRW>;
@@ -118,14 +152,19 @@ __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const R
     uint64_t* cempty = cfull + NS;
     uint64_t* hfull = cempty + NS;
     uint64_t* hempty = hfull + NH;
-    uint64_t* sfull = hempty + NH;
-    uint64_t* sempty = sfull + NSC;
+    uint64_t* sempty = hempty + NH;
+    // per chunk stage: {global chunk number, unit number (-1: stop), chunk of the unit, 0}
+    int4* ctag = reinterpret_cast<int4*>(sempty + NSC);
+    int* stag = reinterpret_cast<int*>(ctag + NS);  // per scratch slot: unit number prepared in it
+    int* htag = stag + NSC;                          // per head stage: unit number it is being filled with
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&cfull[s], 1), mbar_init(&cempty[s], NRW);
-        for (int s = 0; s < NH; ++s) mbar_init(&hfull[s], 1), mbar_init(&hempty[s], NRW + 1);
-        for (int s = 0; s < NSC; ++s) mbar_init(&sfull[s], 1), mbar_init(&sempty[s], NRW);
+        for (int s = 0; s < NS; ++s) mbar_init(&cfull[s], 1), mbar_init(&cempty[s], 1);
+        for (int s = 0; s < NH; ++s) mbar_init(&hfull[s], 1), mbar_init(&hempty[s], p.nchunk + 2);
+        for (int s = 0; s < NSC; ++s) mbar_init(&sempty[s], p.nchunk), stag[s] = -1;
+        for (int s = 0; s < NS; ++s) ctag[s] = make_int4(-1, -1, 0, 0);
+        for (int s = 0; s < NH; ++s) htag[s] = -1;
         fence_barrier_init();
     }
     __syncthreads();
@@ -204,6 +243,7 @@ __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const R
                         meta->slot = s_i, meta->count = c_i, meta->fold = f_i, meta->pos0 = p_i, meta->ckpt0 = k_i;
 #pragma unroll
                         for (int t = 0; t < TMAX; ++t) meta->alpha[t] = al_i[t], meta->beta[t] = be_i[t];
+                        *reinterpret_cast<volatile int*>(htag + hs) = n;  // before the stage is armed
                         if (s_i >= 0)
                             mbar_arrive_expect_tx(&hfull[hs], T * (2 * qbytes + vbytes) + c_i * (qbytes + recbytes));
                         else
@@ -263,25 +303,43 @@ __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const R
             const int unit = blockIdx.x + n * gridDim.x;
             if (unit >= total) break;
             const int hs = n % NH;
-            if (!(ok = __all_sync(FULL_MASK, mbar_wait(&hfull[hs], (n / NH) & 1)))) break;
+            if (!(ok = __all_sync(FULL_MASK, wait_tag(htag + hs, n) && mbar_wait(&hfull[hs], (n / NH) & 1)))) break;
             const int slot = reinterpret_cast<const ReplayMeta*>(heads + hs * p.head_bytes)->slot;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hempty[hs]);  // done reading the unit's metadata
             if (slot < 0) continue;
             const int h = unit % p.Hv;
-            if (lane < p.nchunk) {
-                const uint32_t mc = m + lane;
+            // at most NS lanes at a time, so no lane waits for a stage another lane is about to fill
+            for (int c0 = 0; c0 < p.nchunk && ok; c0 += NS) {
+                const int c = c0 + lane;
+                if (lane < NS && c < p.nchunk) {
+                    const uint32_t mc = m + c;
+                    const int cs = mc % NS;
+                    ok = mc < (uint32_t)NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
+                    if (ok) {
+                        const char* src = static_cast<const char*>(p.ckpt) +
+                                          ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)c * cbytes;
+                        ctag[cs] = make_int4(mc, n, c, 0);
+                        mbar_arrive_expect_tx(&cfull[cs], cbytes);
+                        bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                    }
+                }
+                ok = __all_sync(FULL_MASK, ok);
+            }
+            m += p.nchunk;
+        }
+        if (ok && lane == 0) {  // one stop tag per row warp, posted in order by one lane
+            for (int i = 0; i < NRW && ok; ++i) {
+                const uint32_t mc = m + i;
                 const int cs = mc % NS;
                 ok = mc < (uint32_t)NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
                 if (ok) {
-                    const char* src = static_cast<const char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES +
-                                      (int64_t)lane * cbytes;
-                    mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                    bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                    ctag[cs] = make_int4(mc, -1, 0, 0);
+                    mbar_arrive(&cfull[cs]);
                 }
             }
-            ok = __all_sync(FULL_MASK, ok);
-            m += p.nchunk;
         }
-        if (!ok && lane == 0) {
+        if (!__all_sync(FULL_MASK, ok) && lane == 0) {
             set_error(p.dev_err, GDN_DEVERR_TIMEOUT);
             for (uint32_t s = 0; s < (uint32_t)NS && s < m; ++s) mbar_wait(&cfull[s], ((m - 1 - s) / NS) & 1);
         }
@@ -296,155 +354,205 @@ __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const R
             const int unit = blockIdx.x + n * gridDim.x;
             if (unit >= total) break;
             const int hs = n % NH, ss = n % NSC;
-            if (!(ok = mbar_wait(&hfull[hs], (n / NH) & 1))) break;
+            // the head stage may still hold an older unit's fill: wait for this unit's tag first
+            if (!(ok = wait_tag(htag + hs, n) && mbar_wait(&hfull[hs], (n / NH) & 1))) break;
             if (n >= NSC && !(ok = mbar_wait(&sempty[ss], ((n / NSC) + 1) & 1))) break;
             const unsigned char* head = heads + hs * p.head_bytes;
             const ReplayMeta* meta = reinterpret_cast<const ReplayMeta*>(head);
             const int slot = meta->slot;
-            if (slot >= 0) {
-                unsigned char* scr = smem + p.scratch_off + ss * p.scratch_bytes;
-                float* kw = reinterpret_cast<float*>(scr + p.off_kw);      // [TMAX][DK] window keys
-                float* qw = reinterpret_cast<float*>(scr + p.off_qw);      // [TMAX][DK] window queries
-                float* khat = reinterpret_cast<float*>(scr + p.off_khat);  // [L][DK] ring keys (fold only)
-                float* ckk = reinterpret_cast<float*>(scr + p.off_coef);   // [TMAX][LT]
-                float* ckq = ckk + TMAX * LT;                              // [TMAX][LT]
-                float* G1 = ckq + TMAX * LT;                               // [TMAX]
-                float* G2 = G1 + TMAX;                                     // [TMAX]
-                float* Gf = G2 + TMAX;                                     // [1]
-                float* cf = Gf + 1;                                        // [L]
-                const int count = meta->count, fold = meta->fold, pos0 = meta->pos0;
-                const int cpr = fold ? 0 : count;  // ring entries in front of the window
-                const float* rec = reinterpret_cast<const float*>(head + p.off_rec);
-                const int b = unit / p.Hv, h = unit - b * p.Hv;
-                const int64_t unit_ring = ((int64_t)slot * p.Hv + h) * L;
-
-                // window keys and queries, normalised; lane holds elements lane + 32 m
-                float kwr[TMAX][C::PE], qwr[TMAX][C::PE];
-#pragma unroll
-                for (int t = 0; t < TMAX; ++t) {
-                    float ssk = 0.f, ssq = 0.f;
-#pragma unroll
-                    for (int m = 0; m < C::PE; ++m) {
-                        const int i = lane + 32 * m;
-                        kwr[t][m] = t < T ? load_elem(head + p.off_wk + t * DK * in_sz, i, p.in_dtype) : 0.f;
-                        qwr[t][m] = t < T ? load_elem(head + p.off_wq + t * DK * in_sz, i, p.in_dtype) : 0.f;
-                        ssk = fmaf(kwr[t][m], kwr[t][m], ssk);
-                        ssq = fmaf(qwr[t][m], qwr[t][m], ssq);
-                    }
-                    if (t < T) {
-                        const float ik = rsqrtf(warp_sum(ssk) + 1e-6f);
-                        const float iq = rsqrtf(warp_sum(ssq) + 1e-6f) * p.q_scale;
-#pragma unroll
-                        for (int m = 0; m < C::PE; ++m) {
-                            kwr[t][m] *= ik, qwr[t][m] *= iq;
-                            kw[t * DK + lane + 32 * m] = kwr[t][m];
-                            qw[t * DK + lane + 32 * m] = qwr[t][m];
-                        }
-                    }
-                }
-                // window-window dots (entries cpr + s): k_s.k_t for s < t, k_s.q_t for s <= t
-#pragma unroll
-                for (int t = 0; t < TMAX; ++t) {
-#pragma unroll
-                    for (int s = 0; s <= t; ++s) {
-                        if (t < T) {
-                            float dkk = 0.f, dkq = 0.f;
-#pragma unroll
-                            for (int m = 0; m < C::PE; ++m)
-                                dkk = fmaf(kwr[s][m], kwr[t][m], dkk), dkq = fmaf(kwr[s][m], qwr[t][m], dkq);
-                            dkk = warp_sum(dkk);
-                            dkq = warp_sum(dkq);
-                            if (lane == 0) {
-                                if (s < t) ckk[t * LT + cpr + s] = dkk;
-                                ckq[t * LT + cpr + s] = dkq;
-                            }
-                        }
-                    }
-                }
-                // buffered ring entries: norms, and dots with the window (or normalised keys for a fold)
-                const unsigned char* rk = head + p.off_rk;
-                for (int f = 0; f < count; ++f) {
-                    float x[C::PE], ss2 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < C::PE; ++m) {
-                        x[m] = load_elem(rk + f * DK * in_sz, lane + 32 * m, p.in_dtype);
-                        ss2 = fmaf(x[m], x[m], ss2);
-                    }
-                    const float ik = rsqrtf(warp_sum(ss2) + 1e-6f);
-                    if (fold) {
-#pragma unroll
-                        for (int m = 0; m < C::PE; ++m) khat[f * DK + lane + 32 * m] = x[m] * ik;
-                    } else {
-#pragma unroll
-                        for (int t = 0; t < TMAX; ++t) {
-                            if (t < T) {
-                                float dkk = 0.f, dkq = 0.f;
-#pragma unroll
-                                for (int m = 0; m < C::PE; ++m)
-                                    dkk = fmaf(x[m], kwr[t][m], dkk), dkq = fmaf(x[m], qwr[t][m], dkq);
-                                dkk = warp_sum(dkk);
-                                dkq = warp_sum(dkq);
-                                if (lane == 0) ckk[t * LT + f] = dkk * ik, ckq[t * LT + f] = dkq * ik;
-                            }
-                        }
+            const int b = unit / p.Hv, h = unit - b * p.Hv;
+            if (slot < 0) {
+                // no chunks will come for this unit: zero its outputs and release on the rows' behalf
+                if (slot == -1 && T > 0) {
+                    for (int x = lane; x < T * p.dv; x += 32) {
+                        const int t = x / p.dv, j = x - t * p.dv;
+                        store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, 0.f);
                     }
                 }
                 __syncwarp();
-                // decay products. Entry e (post-fold numbering): e < cpr ring entry, else window
-                // token e - cpr. Item f = -1 gives G(e); f >= 0 scales the dot products by A(f, .).
-                const int etot = cpr + T;
-                for (int f = lane - 1; f < etot; f += 32) {
-                    float prod = 1.f;  // A(f, e - 1) at the top of iteration e
-                    for (int e = f + 1; e < etot; ++e) {
-                        const int t = e - cpr;
-                        if (t >= 0) {
-                            if (f >= 0)
-                                ckk[t * LT + f] *= prod;
-                            else
-                                G1[t] = prod;
-                        }
-                        prod *= e < cpr ? rec[e * rec_floats] : meta->alpha[t];
-                        if (t >= 0) {
-                            if (f >= 0)
-                                ckq[t * LT + f] *= prod;
-                            else
-                                G2[t] = prod;
-                        }
-                    }
-                }
-                if (fold) {  // fold coefficients over the pre-fold ring entries 0..count-1
-                    for (int f = lane - 1; f < count; f += 32) {
-                        float prod = 1.f;
-                        for (int e = f + 1; e < count; ++e) prod *= rec[e * rec_floats];
-                        if (f >= 0)
-                            cf[f] = prod;
-                        else
-                            Gf[0] = prod;
-                    }
-                }
-                // append the window's raw inputs and gates to the ring; move the pointers
-                const int kvec = DK * in_sz / 16, vvec = p.dv * in_sz / 16;
-                for (int t = 0; t < T; ++t) {
-                    const int64_t ent = unit_ring + (pos0 + t) % L;
-                    for (int x = lane; x < kvec; x += 32)
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * DK * in_sz)[x] =
-                            reinterpret_cast<const uint4*>(head + p.off_wk + t * DK * in_sz)[x];
-                    for (int x = lane; x < vvec; x += 32)
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz)[x] =
-                            reinterpret_cast<const uint4*>(head + p.off_wv + t * p.dv * in_sz)[x];
-                    if (lane == 0)
-                        *reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats) =
-                            make_float4(meta->alpha[t], meta->beta[t], 0.f, 0.f);
-                }
                 if (lane == 0) {
-                    const int64_t idx = (int64_t)slot * p.Hv + h;
-                    p.pos[idx] = pos0 + T;
-                    if (fold) p.ckpt_pos[idx] = pos0;
+                    mbar_arrive_n(&sempty[ss], p.nchunk);
+                    mbar_arrive_n(&hempty[hs], p.nchunk + 1);
+                }
+                continue;
+            }
+            unsigned char* scr = smem + p.scratch_off + ss * p.scratch_bytes;
+            float* kw = reinterpret_cast<float*>(scr + p.off_kw);      // [TMAX][DK] window keys
+            float* qw = reinterpret_cast<float*>(scr + p.off_qw);      // [TMAX][DK] window queries
+            float* ckk = reinterpret_cast<float*>(scr + p.off_coef);   // [TMAX][LT]
+            float* ckq = ckk + TMAX * LT;                              // [TMAX][LT]
+            float* G1 = ckq + TMAX * LT;                               // [TMAX]
+            float* G2 = G1 + TMAX;                                     // [TMAX]
+            float* Gf = G2 + TMAX;                                     // [1]
+            float* cf = Gf + 1;                                        // [L]
+            const int count = meta->count, fold = meta->fold, pos0 = meta->pos0;
+            const int cpr = fold ? 0 : count;  // ring entries in front of the window
+            const float* rec = reinterpret_cast<const float*>(head + p.off_rec);
+            const int64_t unit_ring = ((int64_t)slot * p.Hv + h) * L;
+            // Lane groups as in the row warps: LPR lanes per vector, E elements per lane at
+            // positions (cc * LPR + pg) * VEC + e; RPP vectors per warp pass.
+            const int pg = lane % C::LPR, rsub = lane / C::LPR;
+            auto pos_of = [&](int cc) { return (cc * C::LPR + pg) * C::VEC; };
+
+            // window keys and queries, normalised; every group holds the whole vectors
+            float kwn[C::KW_REG ? TMAX : 1][C::E], qwn[C::KW_REG ? TMAX : 1][C::E], ikw[TMAX];
+            constexpr int KWN = C::KW_REG ? TMAX : 1;
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+                ikw[t] = 0.f;
+                if (t < T) {
+                    float xk[C::E], xq[C::E], ssk = 0.f, ssq = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < C::NC; ++cc) {
+                        load_run<C::VEC>(head + p.off_wk + t * DK * in_sz, pos_of(cc), p.in_dtype, xk + cc * C::VEC);
+                        load_run<C::VEC>(head + p.off_wq + t * DK * in_sz, pos_of(cc), p.in_dtype, xq + cc * C::VEC);
+                    }
+#pragma unroll
+                    for (int e = 0; e < C::E; ++e) ssk = fmaf(xk[e], xk[e], ssk), ssq = fmaf(xq[e], xq[e], ssq);
+                    const float ik = rsqrtf(group_sum<C::LPR>(ssk) + 1e-6f);
+                    const float iq = rsqrtf(group_sum<C::LPR>(ssq) + 1e-6f) * p.q_scale;
+                    ikw[t] = ik;
+#pragma unroll
+                    for (int e = 0; e < C::E; ++e) xk[e] *= ik, xq[e] *= iq;
+                    if (rsub == 0) {
+#pragma unroll
+                        for (int cc = 0; cc < C::NC; ++cc) {
+#pragma unroll
+                            for (int u = 0; u < C::VEC; u += 4) {
+                                const int e0 = cc * C::VEC + u;
+                                *reinterpret_cast<float4*>(kw + t * DK + pos_of(cc) + u) =
+                                    make_float4(xk[e0], xk[e0 + 1], xk[e0 + 2], xk[e0 + 3]);
+                                *reinterpret_cast<float4*>(qw + t * DK + pos_of(cc) + u) =
+                                    make_float4(xq[e0], xq[e0 + 1], xq[e0 + 2], xq[e0 + 3]);
+                            }
+                        }
+                    }
+                    if (C::KW_REG) {
+#pragma unroll
+                        for (int e = 0; e < C::E; ++e) kwn[t < KWN ? t : 0][e] = xk[e], qwn[t < KWN ? t : 0][e] = xq[e];
+                    }
                 }
             }
             __syncwarp();
+            // window vector t at this lane's positions (registers, or the scratch table for wide windows)
+            auto wk = [&](int t, int e) -> float {
+                return C::KW_REG ? kwn[t < KWN ? t : 0][e] : kw[t * DK + pos_of(e / C::VEC) + e % C::VEC];
+            };
+            auto wq = [&](int t, int e) -> float {
+                return C::KW_REG ? qwn[t < KWN ? t : 0][e] : qw[t * DK + pos_of(e / C::VEC) + e % C::VEC];
+            };
+            // window-window dot products (entries cpr + s): k_s.k_t for s < t, k_s.q_t for s <= t,
+            // times the window decays between them
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+#pragma unroll
+                for (int s = 0; s <= t; ++s) {
+                    if (t < T) {
+                        float dkk = 0.f, dkq = 0.f;
+#pragma unroll
+                        for (int e = 0; e < C::E; ++e) dkk = fmaf(wk(s, e), wk(t, e), dkk), dkq = fmaf(wk(s, e), wq(t, e), dkq);
+                        dkk = group_sum<C::LPR>(dkk);
+                        dkq = group_sum<C::LPR>(dkq);
+                        if (lane == 0) {
+                            float dec = 1.f;  // prod_{s < x < t} alpha_x
+                            for (int x = s + 1; x < t; ++x) dec *= meta->alpha[x];
+                            if (s < t) ckk[t * LT + cpr + s] = dkk * dec;
+                            ckq[t * LT + cpr + s] = dkq * dec * (s < t ? meta->alpha[t] : 1.f);
+                        }
+                    }
+                }
+            }
+            // buffered ring entries, RPP per warp pass: dot products with the window (scaled by the
+            // entry's cached inverse norm), or the normalised key for a fold
+            for (int f0 = 0; f0 < count; f0 += C::RPP) {
+                const int f = min(f0 + rsub, count - 1);
+                const float ik_f = rec[f * rec_floats + 2];
+                float x[C::E];
+#pragma unroll
+                for (int cc = 0; cc < C::NC; ++cc)
+                    load_run<C::VEC>(head + p.off_rk + f * DK * in_sz, pos_of(cc), p.in_dtype, x + cc * C::VEC);
+                if (fold) {
+                    // a fold reads the raw ring keys from the head stage with the cached inverse norms
+                } else {
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) {
+                        if (t < T) {
+                            float2 a2 = make_float2(0.f, 0.f), b2 = a2;
+#pragma unroll
+                            for (int e = 0; e < C::E / 2; ++e) {
+                                const float2 x2 = make_float2(x[2 * e], x[2 * e + 1]);
+                                a2 = __ffma2_rn(x2, make_float2(wk(t, 2 * e), wk(t, 2 * e + 1)), a2);
+                                b2 = __ffma2_rn(x2, make_float2(wq(t, 2 * e), wq(t, 2 * e + 1)), b2);
+                            }
+                            const float dkk = group_sum<C::LPR>(a2.x + a2.y);
+                            const float dkq = group_sum<C::LPR>(b2.x + b2.y);
+                            if (pg == 0 && f0 + rsub < count) ckk[t * LT + f] = dkk * ik_f, ckq[t * LT + f] = dkq * ik_f;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            // decay products, one lane per ring entry: R(f) = prod_{f<g<count} alpha_g by a suffix scan
+            const bool mine = lane < count;
+            float suf = mine ? rec[lane * rec_floats] : 1.f;  // inclusive suffix product
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_down_sync(FULL_MASK, suf, off);
+                if (lane + off < 32) suf *= o;
+            }
+            const float gring = __shfl_sync(FULL_MASK, suf, 0);  // prod of all ring alphas
+            float R = __shfl_down_sync(FULL_MASK, suf, 1);
+            if (lane == 31) R = 1.f;
             if (lane == 0) {
-                mbar_arrive(&sfull[ss]);
+                float wp = 1.f;  // prod of window alphas before token t
+                for (int t = 0; t < T; ++t) {
+                    G1[t] = (fold ? 1.f : gring) * wp;
+                    wp *= meta->alpha[t];
+                    G2[t] = (fold ? 1.f : gring) * wp;
+                }
+                if (fold) Gf[0] = gring;
+            }
+            if (mine) {
+                if (fold) {
+                    cf[lane] = R;
+                } else {
+                    float wp = 1.f;  // A(f, cpr + t - 1) = R(f) * prod_{s<t} alpha_s
+                    for (int t = 0; t < T; ++t) {
+                        ckk[t * LT + lane] *= R * wp;
+                        wp *= meta->alpha[t];
+                        ckq[t * LT + lane] *= R * wp;
+                    }
+                }
+            }
+            // append the window's raw inputs, gates and key norms to the ring; move the pointers
+            const int kvec = DK * in_sz / 16, vvec = p.dv * in_sz / 16;
+            for (int t = 0; t < T; ++t) {
+                const int64_t ent = unit_ring + (pos0 + t) % L;
+                for (int x = lane; x < kvec; x += 32)
+                    reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * DK * in_sz)[x] =
+                        reinterpret_cast<const uint4*>(head + p.off_wk + t * DK * in_sz)[x];
+                for (int x = lane; x < vvec; x += 32)
+                    reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz)[x] =
+                        reinterpret_cast<const uint4*>(head + p.off_wv + t * p.dv * in_sz)[x];
+            }
+            if (lane < T) {
+                float ikt = ikw[0];
+#pragma unroll
+                for (int t = 1; t < TMAX; ++t)
+                    if (lane == t) ikt = ikw[t];
+                const int64_t ent = unit_ring + (pos0 + lane) % L;
+                *reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats) =
+                    make_float4(meta->alpha[lane], meta->beta[lane], ikt, 0.f);
+            }
+            if (lane == 0) {
+                const int64_t idx = (int64_t)slot * p.Hv + h;
+                p.pos[idx] = pos0 + T;
+                if (fold) p.ckpt_pos[idx] = pos0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();  // scratch contents before the tag
+                *reinterpret_cast<volatile int*>(stag + ss) = n;
                 mbar_arrive(&hempty[hs]);
             }
         }
@@ -456,173 +564,264 @@ __global__ void __launch_bounds__((2 + NPW + NRW) * 32, 1) replay_kernel(const R
     const int rw = warp - 2 - NPW;
     const int pg = lane % C::LPR;
     const int rsub = lane / C::LPR;
-    const int passes = p.rows / C::RPP;
-    uint32_t m = 0;
     bool ok = true;
-    for (int n = 0; ok; ++n) {
-        const int unit = blockIdx.x + n * gridDim.x;
-        if (unit >= total) break;
+    for (uint32_t m = rw;; m += NRW) {
+        const int cs = m % NS;
+        // the stage's tag names the chunk first, so an older round of the stage is never taken for it
+        if (!(ok = wait_tag(&ctag[cs].x, (int)m) && mbar_wait(&cfull[cs], (m / NS) & 1))) break;
+        const int4 tag = ctag[cs];
+        if (tag.y < 0) {  // stop: release the stage (a later stop tag may need it) and leave
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cempty[cs]);
+            break;
+        }
+        const int n = tag.y, c = tag.z;
         const int hs = n % NH, ss = n % NSC;
-        if (!(ok = mbar_wait(&sfull[ss], (n / NSC) & 1) && mbar_wait(&hfull[hs], (n / NH) & 1))) break;
+        if (!(ok = wait_tag(stag + ss, n) && mbar_wait(&hfull[hs], (n / NH) & 1))) break;
+        __threadfence_block();  // scratch contents after the tag
+        const int unit = blockIdx.x + n * gridDim.x;
         const unsigned char* head = heads + hs * p.head_bytes;
         const ReplayMeta* meta = reinterpret_cast<const ReplayMeta*>(head);
         const int slot = meta->slot;
         const int b = unit / p.Hv, h = unit - b * p.Hv;
-        if (slot >= 0) {
-            const int count = meta->count, fold = meta->fold, pos0 = meta->pos0;
-            const int cpr = fold ? 0 : count;
-            const int64_t unit_ring = ((int64_t)slot * p.Hv + h) * L;
-            const float* rec = reinterpret_cast<const float*>(head + p.off_rec);
-            const unsigned char* scr = smem + p.scratch_off + ss * p.scratch_bytes;
-            const float* kwp = reinterpret_cast<const float*>(scr + p.off_kw);
-            const float* qwp = reinterpret_cast<const float*>(scr + p.off_qw);
-            const float* khat = reinterpret_cast<const float*>(scr + p.off_khat);
-            const float* ckk = reinterpret_cast<const float*>(scr + p.off_coef);
-            const float* ckq = ckk + TMAX * LT;
-            const float* G1 = ckq + TMAX * LT;
-            const float* G2 = G1 + TMAX;
-            const float gfold = fold ? G2[TMAX] : 1.f;  // Gf follows G2
-            const float* cf = G2 + TMAX + 1;
+        const int count = meta->count, fold = meta->fold, pos0 = meta->pos0;
+        const int cpr = fold ? 0 : count;
+        const int64_t unit_ring = ((int64_t)slot * p.Hv + h) * L;
+        const float* rec = reinterpret_cast<const float*>(head + p.off_rec);
+        const unsigned char* scr = smem + p.scratch_off + ss * p.scratch_bytes;
+        const float* kwp = reinterpret_cast<const float*>(scr + p.off_kw);
+        const float* qwp = reinterpret_cast<const float*>(scr + p.off_qw);
+        const float* ckk = reinterpret_cast<const float*>(scr + p.off_coef);
+        const float* ckq = ckk + TMAX * LT;
+        const float* G1 = ckq + TMAX * LT;
+        const float* G2 = G1 + TMAX;
+        const float gfold = fold ? G2[TMAX] : 1.f;  // Gf follows G2
+        const float* cf = G2 + TMAX + 1;
+        const unsigned char* tile = chunks + cs * CHUNK_BYTES;
+        char* gck = static_cast<char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
 
-            // window vectors at this lane's key positions
-            auto win = [&](const float* base, int t, int c, int u) -> float4 {
-                return *reinterpret_cast<const float4*>(base + t * DK + (c * C::LPR + pg) * C::VEC + u);
-            };
-            constexpr int KWN = C::KW_REG ? TMAX : 1;
-            float kw[KWN][C::E], qw[KWN][C::E];
-            if (C::KW_REG) {
+        // window vectors at this lane's key positions
+        auto win = [&](const float* base, int t, int cc, int u) -> float4 {
+            return *reinterpret_cast<const float4*>(base + t * DK + (cc * C::LPR + pg) * C::VEC + u);
+        };
+        constexpr int KWN = C::KW_REG ? TMAX : 1;
+        float kw[KWN][C::E], qw[KWN][C::E];
+        if (C::KW_REG) {
 #pragma unroll
-                for (int t = 0; t < KWN; ++t) {
+            for (int t = 0; t < KWN; ++t) {
 #pragma unroll
-                    for (int c = 0; c < C::NC; ++c) {
+                for (int cc = 0; cc < C::NC; ++cc) {
 #pragma unroll
-                        for (int u = 0; u < C::VEC; u += 4) {
-                            float4 vk = make_float4(0.f, 0.f, 0.f, 0.f), vq = vk;
-                            if (t < T) vk = win(kwp, t, c, u), vq = win(qwp, t, c, u);
-                            const int e0 = c * C::VEC + u;
-                            kw[t][e0] = vk.x, kw[t][e0 + 1] = vk.y, kw[t][e0 + 2] = vk.z, kw[t][e0 + 3] = vk.w;
-                            qw[t][e0] = vq.x, qw[t][e0 + 1] = vq.y, qw[t][e0 + 2] = vq.z, qw[t][e0 + 3] = vq.w;
-                        }
+                    for (int u = 0; u < C::VEC; u += 4) {
+                        float4 vk = make_float4(0.f, 0.f, 0.f, 0.f), vq = vk;
+                        if (t < T) vk = win(kwp, t, cc, u), vq = win(qwp, t, cc, u);
+                        const int e0 = cc * C::VEC + u;
+                        kw[t][e0] = vk.x, kw[t][e0 + 1] = vk.y, kw[t][e0 + 2] = vk.z, kw[t][e0 + 3] = vk.w;
+                        qw[t][e0] = vq.x, qw[t][e0 + 1] = vq.y, qw[t][e0 + 2] = vq.z, qw[t][e0 + 3] = vq.w;
                     }
                 }
             }
-            char* gck = static_cast<char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
-            for (int c = 0; c < p.nchunk; ++c, ++m) {
-                const int cs = m % NS;
-                if (!(ok = mbar_wait(&cfull[cs], (m / NS) & 1))) break;
-                const unsigned char* tile = chunks + cs * CHUNK_BYTES;
-                // passes of the unit spread over the row warps across chunks
-                for (int ps = ((rw - c * passes) % NRW + NRW) % NRW; ps < passes; ps += NRW) {
-                    const int r = ps * C::RPP + rsub;
-                    const int j = c * p.rows + r;
-                    float s[C::E];
+        }
+
+        // Load one state row of the chunk (this lane's E elements) and fold it if required.
+        auto load_row = [&](int r, float (&s)[C::E]) {
 #pragma unroll
-                    for (int cc = 0; cc < C::NC; ++cc) {
-                        const uint4 raw =
-                            *reinterpret_cast<const uint4*>(tile + r * C::ROW_BYTES + (cc * C::LPR + pg) * 16);
-                        Store<ST>::unpack(raw, s + cc * C::VEC);
-                    }
+            for (int cc = 0; cc < C::NC; ++cc) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(tile + r * C::ROW_BYTES + (cc * C::LPR + pg) * 16);
+                Store<ST>::unpack(raw, s + cc * C::VEC);
+            }
+            if (fold) {
+                // S0 <- round(G S0 + sum_f A(f, count-1) k_f w_f^T), row j
+                const int j = c * p.rows + r;
+#pragma unroll
+                for (int e = 0; e < C::E; ++e) s[e] *= gfold;
+                for (int f = 0; f < count; ++f) {
+                    // k_f = raw key * 1/|k_f| (cached in the record)
+                    const float cwf = cf[f] * rec[f * rec_floats + 4 + j] * rec[f * rec_floats + 2];
+                    float kr[C::E];
+#pragma unroll
+                    for (int cc = 0; cc < C::NC; ++cc)
+                        load_run<C::VEC>(head + p.off_rk + f * DK * in_sz, (cc * C::LPR + pg) * C::VEC, p.in_dtype,
+                                         kr + cc * C::VEC);
+#pragma unroll
+                    for (int e = 0; e < C::E; ++e) s[e] = fmaf(kr[e], cwf, s[e]);
+                }
+                char* dst = gck + (int64_t)j * C::ROW_BYTES;
+#pragma unroll
+                for (int cc = 0; cc < C::NC; ++cc) {
+                    const uint4 packed = Store<ST>::pack(s + cc * C::VEC);
+                    *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = packed;
+                    Store<ST>::unpack(packed, s + cc * C::VEC);  // continue from the stored values
+                }
+            }
+        };
+
+        if (T > 0 && C::FAST) {
+            // window of one token: per 32-row block, LPR passes of partial dots, then a reduce-scatter
+            // leaves lane (rsub, pg) with the sums of row pg * RPP + rsub of the block
+            constexpr int MAXBLK = CHUNK_BYTES / C::ROW_BYTES / 32 > 0 ? CHUNK_BYTES / C::ROW_BYTES / 32 : 1;
+            float2 kw2[C::E / 2], qw2[C::E / 2];
+#pragma unroll
+            for (int e = 0; e < C::E / 2; ++e)
+                kw2[e] = make_float2(kw[0][2 * e], kw[0][2 * e + 1]), qw2[e] = make_float2(qw[0][2 * e], qw[0][2 * e + 1]);
+            const float g1 = G1[0], g2 = G2[0], al = meta->alpha[0], be = meta->beta[0];
+            const float cdiag = ckq[cpr];  // k_t.q_t
+            const int nblk = p.rows / 32;
+            float Yb[MAXBLK], Zb[MAXBLK];
+#pragma unroll
+            for (int blk = 0; blk < MAXBLK; ++blk) {
+                if (blk < nblk) {
+                    const int r0 = blk * 32;
+                    float y[C::LPR], z[C::LPR];
                     if (fold) {
-                        // S0 <- round(G S0 + sum_f A(f, count-1) k_f w_f^T), row j
 #pragma unroll
-                        for (int e = 0; e < C::E; ++e) s[e] *= gfold;
-                        for (int f = 0; f < count; ++f) {
-                            const float cwf = cf[f] * rec[f * rec_floats + 4 + j];
-                            const float* kf = khat + f * DK;
+                        for (int ps = 0; ps < C::LPR; ++ps) {
+                            float s[C::E];
+                            load_row(r0 + ps * C::RPP + rsub, s);
+                            float2 u2 = make_float2(0.f, 0.f), v2 = u2;
+#pragma unroll
+                            for (int e = 0; e < C::E / 2; ++e) {
+                                const float2 s2 = make_float2(s[2 * e], s[2 * e + 1]);
+                                u2 = __ffma2_rn(s2, kw2[e], u2);
+                                v2 = __ffma2_rn(s2, qw2[e], v2);
+                            }
+                            y[ps] = u2.x + u2.y;
+                            z[ps] = v2.x + v2.y;
+                        }
+                    } else {
+                        // 16-byte vector cc of all LPR passes first, then their math: 2*LPR independent chains
+                        float2 u2[C::LPR], v2[C::LPR];
+#pragma unroll
+                        for (int ps = 0; ps < C::LPR; ++ps) u2[ps] = make_float2(0.f, 0.f), v2[ps] = u2[ps];
+#pragma unroll
+                        for (int cc = 0; cc < C::NC; ++cc) {
+                            uint4 raw[C::LPR];
+#pragma unroll
+                            for (int ps = 0; ps < C::LPR; ++ps)
+                                raw[ps] = *reinterpret_cast<const uint4*>(tile + (r0 + ps * C::RPP + rsub) * C::ROW_BYTES +
+                                                                          (cc * C::LPR + pg) * 16);
+#pragma unroll
+                            for (int ps = 0; ps < C::LPR; ++ps) {
+                                float sv[C::VEC];
+                                Store<ST>::unpack(raw[ps], sv);
+#pragma unroll
+                                for (int e = 0; e < C::VEC / 2; ++e) {
+                                    const float2 s2 = make_float2(sv[2 * e], sv[2 * e + 1]);
+                                    u2[ps] = __ffma2_rn(s2, kw2[cc * C::VEC / 2 + e], u2[ps]);
+                                    v2[ps] = __ffma2_rn(s2, qw2[cc * C::VEC / 2 + e], v2[ps]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int ps = 0; ps < C::LPR; ++ps) y[ps] = u2[ps].x + u2[ps].y, z[ps] = v2[ps].x + v2[ps].y;
+                    }
+                    Yb[blk] = reduce_scatter<C::LPR>(y, pg) * g1;
+                    Zb[blk] = reduce_scatter<C::LPR>(z, pg) * g2;
+                }
+            }
+            // the chunk's state rows are consumed: hand the stage back before the per-row tail
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cempty[cs]);
+#pragma unroll
+            for (int blk = 0; blk < MAXBLK; ++blk) {
+                if (blk < nblk) {
+                    const int r = blk * 32 + pg * C::RPP + rsub;
+                    const int j = c * p.rows + r;
+                    float Y = Yb[blk], Z = Zb[blk];
+                    float Y1 = 0.f, Z1 = 0.f, Y2 = 0.f, Z2 = 0.f, Y3 = 0.f, Z3 = 0.f;
+                    int f = 0;
+                    for (; f + 4 <= cpr; f += 4) {
+                        const float w0 = rec[f * rec_floats + 4 + j], w1 = rec[(f + 1) * rec_floats + 4 + j];
+                        const float w2 = rec[(f + 2) * rec_floats + 4 + j], w3 = rec[(f + 3) * rec_floats + 4 + j];
+                        Y = fmaf(ckk[f], w0, Y), Z = fmaf(ckq[f], w0, Z);
+                        Y1 = fmaf(ckk[f + 1], w1, Y1), Z1 = fmaf(ckq[f + 1], w1, Z1);
+                        Y2 = fmaf(ckk[f + 2], w2, Y2), Z2 = fmaf(ckq[f + 2], w2, Z2);
+                        Y3 = fmaf(ckk[f + 3], w3, Y3), Z3 = fmaf(ckq[f + 3], w3, Z3);
+                    }
+                    for (; f < cpr; ++f) {
+                        const float wf = rec[f * rec_floats + 4 + j];
+                        Y = fmaf(ckk[f], wf, Y), Z = fmaf(ckq[f], wf, Z);
+                    }
+                    Y += (Y1 + Y2) + Y3;
+                    Z += (Z1 + Z2) + Z3;
+                    const float vj = load_elem(head + p.off_wv, j, p.in_dtype);
+                    const float ww = be * (vj - al * Y);
+                    store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype, fmaf(cdiag, ww, Z));
+                    p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
+                }
+            }
+        } else {
+            const int passes = p.rows / C::RPP;
+            for (int ps = 0; ps < passes; ++ps) {
+                const int r = ps * C::RPP + rsub;
+                const int j = c * p.rows + r;
+                float s[C::E];
+                load_row(r, s);
+                if (T > 0) {
+                    float y[TMAX], z[TMAX];
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) {
+                        float dy = 0.f, dz = 0.f;
+                        if (C::KW_REG) {
+#pragma unroll
+                            for (int e = 0; e < C::E; ++e)
+                                dy = fmaf(s[e], kw[C::KW_REG ? t : 0][e], dy), dz = fmaf(s[e], qw[C::KW_REG ? t : 0][e], dz);
+                        } else if (t < T) {
 #pragma unroll
                             for (int cc = 0; cc < C::NC; ++cc) {
 #pragma unroll
                                 for (int u = 0; u < C::VEC; u += 4) {
-                                    const float4 kv =
-                                        *reinterpret_cast<const float4*>(kf + (cc * C::LPR + pg) * C::VEC + u);
+                                    const float4 vk = win(kwp, t, cc, u), vq = win(qwp, t, cc, u);
                                     const int e0 = cc * C::VEC + u;
-                                    s[e0] = fmaf(kv.x, cwf, s[e0]), s[e0 + 1] = fmaf(kv.y, cwf, s[e0 + 1]);
-                                    s[e0 + 2] = fmaf(kv.z, cwf, s[e0 + 2]), s[e0 + 3] = fmaf(kv.w, cwf, s[e0 + 3]);
+                                    dy = fmaf(s[e0], vk.x, dy), dy = fmaf(s[e0 + 1], vk.y, dy);
+                                    dy = fmaf(s[e0 + 2], vk.z, dy), dy = fmaf(s[e0 + 3], vk.w, dy);
+                                    dz = fmaf(s[e0], vq.x, dz), dz = fmaf(s[e0 + 1], vq.y, dz);
+                                    dz = fmaf(s[e0 + 2], vq.z, dz), dz = fmaf(s[e0 + 3], vq.w, dz);
                                 }
                             }
                         }
-                        char* dst = gck + (int64_t)j * C::ROW_BYTES;
-#pragma unroll
-                        for (int cc = 0; cc < C::NC; ++cc) {
-                            const uint4 packed = Store<ST>::pack(s + cc * C::VEC);
-                            *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = packed;
-                            Store<ST>::unpack(packed, s + cc * C::VEC);  // continue from the stored values
-                        }
+                        y[t] = t < T ? G1[t] * dy : 0.f;
+                        z[t] = t < T ? G2[t] * dz : 0.f;
                     }
-                    if (T > 0) {
-                        float y[TMAX], z[TMAX];
-#pragma unroll
-                        for (int t = 0; t < TMAX; ++t) {
-                            float dy = 0.f, dz = 0.f;
-                            if (C::KW_REG) {
-#pragma unroll
-                                for (int e = 0; e < C::E; ++e)
-                                    dy = fmaf(s[e], kw[C::KW_REG ? t : 0][e], dy),
-                                    dz = fmaf(s[e], qw[C::KW_REG ? t : 0][e], dz);
-                            } else if (t < T) {
-#pragma unroll
-                                for (int cc = 0; cc < C::NC; ++cc) {
-#pragma unroll
-                                    for (int u = 0; u < C::VEC; u += 4) {
-                                        const float4 vk = win(kwp, t, cc, u), vq = win(qwp, t, cc, u);
-                                        const int e0 = cc * C::VEC + u;
-                                        dy = fmaf(s[e0], vk.x, dy), dy = fmaf(s[e0 + 1], vk.y, dy);
-                                        dy = fmaf(s[e0 + 2], vk.z, dy), dy = fmaf(s[e0 + 3], vk.w, dy);
-                                        dz = fmaf(s[e0], vq.x, dz), dz = fmaf(s[e0 + 1], vq.y, dz);
-                                        dz = fmaf(s[e0 + 2], vq.z, dz), dz = fmaf(s[e0 + 3], vq.w, dz);
-                                    }
-                                }
-                            }
-                            y[t] = t < T ? G1[t] * dy : 0.f;
-                            z[t] = t < T ? G2[t] * dz : 0.f;
-                        }
-                        for (int f = pg; f < cpr; f += C::LPR) {
-                            const float wf = rec[f * rec_floats + 4 + j];
-#pragma unroll
-                            for (int t = 0; t < TMAX; ++t) {
-                                if (t < T) {
-                                    y[t] = fmaf(ckk[t * LT + f], wf, y[t]);
-                                    z[t] = fmaf(ckq[t * LT + f], wf, z[t]);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int t = 0; t < TMAX; ++t) {
-                            y[t] = group_sum<C::LPR>(y[t]);
-                            z[t] = group_sum<C::LPR>(z[t]);
-                        }
-                        float ww[TMAX];
+                    for (int f = pg; f < cpr; f += C::LPR) {
+                        const float wf = rec[f * rec_floats + 4 + j];
 #pragma unroll
                         for (int t = 0; t < TMAX; ++t) {
                             if (t < T) {
-                                float sk = y[t];
+                                y[t] = fmaf(ckk[t * LT + f], wf, y[t]);
+                                z[t] = fmaf(ckq[t * LT + f], wf, z[t]);
+                            }
+                        }
+                    }
 #pragma unroll
-                                for (int x = 0; x < t; ++x) sk = fmaf(ckk[t * LT + cpr + x], ww[x], sk);
-                                const float vj = load_elem(head + p.off_wv + t * p.dv * in_sz, j, p.in_dtype);
-                                ww[t] = meta->beta[t] * (vj - meta->alpha[t] * sk);
-                                float o = z[t];
+                    for (int t = 0; t < TMAX; ++t) {
+                        y[t] = group_sum<C::LPR>(y[t]);
+                        z[t] = group_sum<C::LPR>(z[t]);
+                    }
+                    float ww[TMAX];
 #pragma unroll
-                                for (int x = 0; x <= t; ++x) o = fmaf(ckq[t * LT + cpr + x], ww[x], o);
-                                if (pg == 0) {
-                                    store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, o);
-                                    p.ring_rec[(unit_ring + (pos0 + t) % L) * rec_floats + 4 + j] = ww[t];
-                                }
+                    for (int t = 0; t < TMAX; ++t) {
+                        if (t < T) {
+                            float sk = y[t];
+#pragma unroll
+                            for (int x = 0; x < t; ++x) sk = fmaf(ckk[t * LT + cpr + x], ww[x], sk);
+                            const float vj = load_elem(head + p.off_wv + t * p.dv * in_sz, j, p.in_dtype);
+                            ww[t] = meta->beta[t] * (vj - meta->alpha[t] * sk);
+                            float o = z[t];
+#pragma unroll
+                            for (int x = 0; x <= t; ++x) o = fmaf(ckq[t * LT + cpr + x], ww[x], o);
+                            if (pg == 0) {
+                                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, o);
+                                p.ring_rec[(unit_ring + (pos0 + t) % L) * rec_floats + 4 + j] = ww[t];
                             }
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cempty[cs]);
-            }
-            if (!ok) break;
-        } else if (slot == -1 && T > 0) {
-            for (int x = rw * 32 + lane; x < T * p.dv; x += NRW * 32) {
-                const int t = x / p.dv, j = x - t * p.dv;
-                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, 0.f);
             }
         }
         __syncwarp();
         if (lane == 0) {
+            if (!(T > 0 && C::FAST)) mbar_arrive(&cempty[cs]);
             mbar_arrive(&sempty[ss]);
             mbar_arrive(&hempty[hs]);
         }

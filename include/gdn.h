@@ -42,8 +42,9 @@
  *   - Slot indices are int32; a negative slot is padding: no state is read
  *     or written and the output rows are zero. Slots within one call must be
  *     distinct (not checked; duplicates race).
- *   - Shapes: dk in {32, 64, 128}; dv a multiple of 16 in [16, 256];
- *     Hv a multiple of Hk; B >= 0 (B == 0 launches nothing).
+ *   - Shapes: dk in {32, 64, 128}; dv a multiple of 16 in [16, 256] (of 32
+ *     for the ReplaySSM entry points); Hv a multiple of Hk; B >= 0 (B == 0
+ *     launches nothing).
  */
 #ifndef GDN_H
 #define GDN_H
@@ -113,12 +114,14 @@ int gdn_decode_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype,
  *           layout as a decode state pool. Written only when folded.
  * ring_k    [num_slots][Hv][L][dk] of ring_dtype: raw (unnormalised) keys.
  * ring_v    [num_slots][Hv][L][dv] of ring_dtype: raw values.
- * ring_rec  [num_slots][Hv][L][4 + dv] fp32: per entry {alpha, beta, 0, 0,
- *           w[0..dv)}, where alpha and beta are the entry's gates and
- *           w = beta (v - alpha S_prev^T k) is the entry's correction vector
- *           (S_prev: the state just before the entry). w is derived data the
- *           kernels keep so that an output needs one pass over S0, not one
- *           per buffered entry; it stays valid until the entry is folded.
+ * ring_rec  [num_slots][Hv][L][4 + dv] fp32: per entry {alpha, beta,
+ *           1/|k|, 0, w[0..dv)}, where alpha and beta are the entry's gates,
+ *           1/|k| = 1/sqrt(|k|^2 + 1e-6) its key's inverse norm and
+ *           w = beta (v - alpha S_prev^T k) its correction vector (S_prev:
+ *           the state just before the entry). 1/|k| and w are derived data
+ *           the kernels keep so that an output needs one pass over S0, not
+ *           one per buffered entry; w stays valid until the entry is folded.
+ *           The ring is written only by these entry points.
  * pos       [num_slots][Hv] int32: absolute position of the next token.
  * ckpt_pos  [num_slots][Hv] int32: position the checkpoint corresponds to.
  *           count = pos - ckpt_pos entries are buffered, 0 <= count <= L;

@@ -117,6 +117,7 @@ def test_replay_rejections(lib):
     assert lib.gdn_replay_step(C.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 0, FAKE,
                                None) == -1
     assert lib.gdn_replay_flush(C.byref(_dims(dk=48)), C.byref(_cache()), FAKE, 1, FAKE, None) == -3
+    assert _verify(lib, _dims(dv=48), _cache(), 4) == -3  # replay needs dv % 32 == 0
     assert lib.gdn_rollback(C.byref(d), C.byref(_cache(L=4)), FAKE, FAKE, 5, FAKE, None) == -4
     assert lib.gdn_rollback(C.byref(d), C.byref(_cache()), FAKE, None, 4, FAKE, None) == -1
 

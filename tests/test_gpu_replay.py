@@ -123,7 +123,7 @@ def test_replay_multi_round_with_offsets(sdt, idt):
     H.check_state()
 
 
-@pytest.mark.parametrize("dk,dv", [(64, 48), (128, 256), (32, 96)])
+@pytest.mark.parametrize("dk,dv", [(64, 32), (128, 256), (32, 96), (64, 64)])
 def test_replay_other_head_shapes(dk, dv):
     w = wl.Workload("rh", B=5, Hk=2, Hv=4, dk=dk, dv=dv, steps=9, state_dtype="f32", in_dtype="bf16", L=4, seed=23)
     H = Harness(w)
