@@ -84,15 +84,19 @@ def kernel_source_hash() -> str:
 def ncu_traffic() -> float | None:
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_b256_fp32state_traffic.json")
+    import re
+
+    path = os.path.join(ROOT, "profiles", "decode_kernel_b256_dram_traffic.md")
     try:
         with open(path) as f:
-            doc = json.load(f)
-    except Exception:
+            text = f.read()
+    except OSError:
         return None
-    if doc.get("kernel_source_sha") != kernel_source_hash():
+    sha = re.search(r"^kernel_source_sha: (\w+)", text, re.M)
+    val = re.search(r"^dram_bytes_per_launch: (\d+)", text, re.M)
+    if not sha or not val or sha.group(1) != kernel_source_hash():
         return None
-    return float(doc["dram_bytes_per_launch"])
+    return float(val.group(1))
 
 
 def pci_bus_id(dev: int) -> str | None:
@@ -252,7 +256,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         "bytes_per_token": bpt,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gdn::decode_kernel<float,128,8,8,4>", "launch_us": launch_ms * 1e3,
+                     "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps, 6 chunk stages)", "launch_us": launch_ms * 1e3,
                      "algorithmic_bytes_per_launch": bpt * B},
         "clocks": clocks,
         "gpu_launches": args.steps,
