@@ -167,6 +167,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks
+
+
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    """Max of x over the ranks of the default process group (timing only)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, elapsed_ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (elapsed_ms_max / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 
@@ -202,11 +222,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, dev)
 
     def timed(fn, steps, warmup, per_launch=True):
         """Run warmup, then `steps` timed calls; returns (elapsed ms over ranks, mean launch ms)."""
@@ -242,7 +258,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         elapsed, launch_ms = timed(step, args.steps, 0)
     clocks = sampler.summary()
     bpt = decode_bytes_per_token(4)
-    tok_s = world * B * args.steps / (elapsed / 1e3)
+    tok_s = job_tokens_per_s(B * args.steps, elapsed, world)
     achieved = bpt * B / (launch_ms / 1e3) / 1e9
     result.update({
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
