@@ -375,7 +375,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_decode_rate(seconds: float = 2.0, sample_seqs: int = 32) -> dict:
+def oracle_decode_rate(seconds: float = 15.0, sample_seqs: int = 32) -> dict:
     """Time the CPU oracle on a bounded sample of the headline workload:
     `sample_seqs` sequences x all 32 heads per step, steps repeated until
     `seconds` of wall time, all host cores."""
@@ -394,7 +394,7 @@ def oracle_decode_rate(seconds: float = 2.0, sample_seqs: int = 32) -> dict:
     x0 = wl.step_inputs(w, 0)
     ts = time.perf_counter()
     run(x0)  # calibration step
-    steps = int(min(50, max(1, seconds / max(time.perf_counter() - ts, 1e-6))))
+    steps = int(min(2000, max(1, seconds / max(time.perf_counter() - ts, 1e-6))))
     xs = [wl.step_inputs(w, s) for s in range(1, steps + 1)]
     ts = time.perf_counter()
     for x in xs:

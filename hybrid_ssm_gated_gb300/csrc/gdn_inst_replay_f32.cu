@@ -1,6 +1,6 @@
 // Instantiations of the replay kernel for f32 checkpoints (dk x window size).
 #include "gdn_dispatch.h"
-#include "gdn_launch.cuh"
+#include "gdn_launch_replay.cuh"
 
 namespace gdn {
 

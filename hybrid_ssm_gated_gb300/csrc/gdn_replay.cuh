@@ -92,7 +92,7 @@ struct ReplayArgs {
     float q_scale;
     // shared-memory layout, bytes
     int head_bytes, off_wq, off_wk, off_wv, off_rk, off_rec, off_coef;  // inside a head stage
-    int heads_off, bars_off;                                            // inside the CTA's buffer
+    int heads_off, sums_off, bars_off;                                  // inside the CTA's buffer
 };
 
 constexpr int REPLAY_META = 128;  // bytes of per-unit metadata at the start of a head stage
@@ -104,21 +104,23 @@ struct ReplayCfg {
     static constexpr int NC = E / VEC;
     static constexpr int LPR = DK / E;                  // lanes per row
     static constexpr int RPP = 32 / LPR;                // rows per warp pass
-    // rows per consumer work item: LPR passes for one token (one reduce-scatter makes every lane own
-    // a row), one pass for wider windows (their rows are spread over all consumer warps)
-    static constexpr int PPI = TMAX == 1 ? LPR : 1;
+    // a consumer work item is LPR warp passes = 32 rows, after which every lane owns one row: for
+    // one token through a reduce-scatter of the item's sums, for wider windows through a per-warp
+    // shared-memory tile of the row sums
+    static constexpr int PPI = LPR;
     static constexpr int ITEM = PPI * RPP;
+    static constexpr int SUMS = TMAX == 1 ? 0 : 32 * (2 * TMAX + 1);  // floats of a warp's row-sum tile
     static constexpr int V = 2 * TMAX;                  // sums per row: S^T k_t and S^T q_t
     static constexpr int NVL = V >= LPR ? V / LPR : 1;  // sums a lane holds after the reduce-scatter
     static constexpr int DUP = V >= LPR ? 1 : LPR / V;  // lanes holding the same sum
     static constexpr int FP = 2;                        // rows a lane folds at once (key reuse)
-    // a fold unit's items are split further (one token: SUB sub-items of FP passes), so that its
-    // extra work spreads over all warps; chunk releases count in sub-items
-    static constexpr int SUB = TMAX == 1 ? PPI / FP : 1;
+    // a fold unit's items are split further (SUB sub-items of FP passes), so that its extra work
+    // spreads over all warps; chunk releases count in sub-items
+    static constexpr int SUB = PPI / FP;
     static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
     static constexpr int THREADS = (NCW + 1) * 32;
     static_assert(E % VEC == 0 && DK % E == 0 && LPR >= 2 && LPR <= 32, "unsupported dk");
-    static_assert(TMAX > 1 || PPI % FP == 0, "fold blocking");
+    static_assert(PPI % FP == 0 && ITEM == 32, "item blocking");
 };
 
 // Per-unit metadata written by the producer at the start of a head stage.
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
     const int cw = warp - 1;
     const int pg = lane % C::LPR;    // lane's position within its row group
     const int rsub = lane / C::LPR;  // row group within the warp
-    const int gbase = lane - pg;     // first lane of the group
+    float* sums = reinterpret_cast<float*>(smem + p.sums_off) + cw * C::SUMS;  // this warp's row-sum tile
     auto pos_of = [&](int cc) { return (cc * C::LPR + pg) * C::VEC; };
     // index of the i-th sum this lane holds after reduce_scatter_values
     auto held = [&](int i) { return C::V >= C::LPR ? pg * C::NVL + i : pg / C::DUP; };
@@ -760,76 +762,98 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                             p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                         }
                     } else {
-                        // one pass (RPP rows); the 2T sums of a row are scattered over its lanes
-                        for (int ps = 0; ps < C::PPI; ++ps) {
-                            const int r = r0 + ps * C::RPP + rsub;
-                            const int j = j0 + ps * C::RPP + rsub;
-                            float s1[1][C::E];
-                            load_state(tile, r, s1[0]);
-                            if (fold) {
-                                const int j1[1] = {j};
-                                fold_rows(s1, j1);
-                            }
-                            if (T > 0) {
-                                float v[C::V];
-                                float G1 = g1;  // decay of S0 to token t: g1 prod_{y<t} alpha_y
+                        // Passes of RPP rows: the 2T sums of a row are reduce-scattered over its
+                        // lanes and parked in this warp's tile, one tile row per state row; then one
+                        // lane per row runs the window's recursion and stores the row's outputs.
+                        const int np = fold ? C::FP : C::PPI;                    // passes of this (sub-)item
+                        const int ps0 = fold ? (it - bi * C::SUB) * C::FP : 0;  // its first pass
+                        // two passes at a time (np is even): their loads, FMA chains and shuffles interleave
+                        for (int q = 0; q < np; q += 2) {
+                            float s2[2][C::E];
+                            int jr[2];
 #pragma unroll
-                                for (int t = 0; t < TMAX; ++t) {
+                            for (int r = 0; r < 2; ++r) {
+                                load_state(tile, r0 + (ps0 + q + r) * C::RPP + rsub, s2[r]);
+                                jr[r] = j0 + (ps0 + q + r) * C::RPP + rsub;
+                            }
+                            if (fold) fold_rows(s2, jr);
+                            float v[2][C::V];
+                            float G1 = g1;  // decay of S0 to token t: g1 prod_{y<t} alpha_y
+#pragma unroll
+                            for (int t = 0; t < TMAX; ++t) {
+                                const float G2 = t < T ? G1 * meta->alpha[t] : 0.f;
+#pragma unroll
+                                for (int r = 0; r < 2; ++r) {
                                     float2 a2 = make_float2(0.f, 0.f), b2 = a2;
 #pragma unroll
                                     for (int e = 0; e < C::E / 2; ++e) {
-                                        const float2 s2 = make_float2(s1[0][2 * e], s1[0][2 * e + 1]);
-                                        a2 = __ffma2_rn(s2, kw2[t][e], a2);
-                                        b2 = __ffma2_rn(s2, qw2[t][e], b2);
+                                        const float2 x2 = make_float2(s2[r][2 * e], s2[r][2 * e + 1]);
+                                        a2 = __ffma2_rn(x2, kw2[t][e], a2);
+                                        b2 = __ffma2_rn(x2, qw2[t][e], b2);
                                     }
-                                    const float G2 = t < T ? G1 * meta->alpha[t] : 0.f;
-                                    v[t] = (a2.x + a2.y) * G1;
-                                    v[TMAX + t] = (b2.x + b2.y) * G2;
-                                    G1 = G2;
+                                    v[r][t] = (a2.x + a2.y) * G1;
+                                    v[r][TMAX + t] = (b2.x + b2.y) * G2;
                                 }
+                                G1 = G2;
+                            }
+                            if (cpr > 0) {
                                 if (!have_coef && !(ok = mbar_wait(&cready[hs], hph))) break;
                                 have_coef = true;
                                 // ring terms, split over the row's lanes before the reduction
                                 for (int f = pg; f < cpr; f += C::LPR) {
-                                    const float wf = rec[f * rec_floats + 4 + j];
+                                    const float w0 = rec[f * rec_floats + 4 + jr[0]];
+                                    const float w1 = rec[f * rec_floats + 4 + jr[1]];
 #pragma unroll
                                     for (int i = 0; i < C::V; i += 4) {
                                         const float4 c4 = *reinterpret_cast<const float4*>(coef + f * C::V + i);
-                                        v[i] = fmaf(c4.x, wf, v[i]), v[i + 1] = fmaf(c4.y, wf, v[i + 1]);
-                                        v[i + 2] = fmaf(c4.z, wf, v[i + 2]), v[i + 3] = fmaf(c4.w, wf, v[i + 3]);
+                                        v[0][i] = fmaf(c4.x, w0, v[0][i]), v[0][i + 1] = fmaf(c4.y, w0, v[0][i + 1]);
+                                        v[0][i + 2] = fmaf(c4.z, w0, v[0][i + 2]), v[0][i + 3] = fmaf(c4.w, w0, v[0][i + 3]);
+                                        v[1][i] = fmaf(c4.x, w1, v[1][i]), v[1][i + 1] = fmaf(c4.y, w1, v[1][i + 1]);
+                                        v[1][i + 2] = fmaf(c4.z, w1, v[1][i + 2]), v[1][i + 3] = fmaf(c4.w, w1, v[1][i + 3]);
                                     }
                                 }
-                                reduce_scatter_values<C::V, C::LPR>(v, pg);
-                                // the window's own recursion: w_x from the lane holding S^T k_x, then its
-                                // terms into every later sum of the row (the table holds zeros elsewhere)
+                            }
+                            reduce_scatter_values<C::V, C::LPR>(v[0], pg);
+                            reduce_scatter_values<C::V, C::LPR>(v[1], pg);
+                            if (pg % C::DUP == 0) {
 #pragma unroll
-                                for (int x = 0; x < TMAX; ++x) {
-                                    if (x < T) {
-                                        const int opos = C::V >= C::LPR ? x / C::NVL : x * C::DUP;
-                                        const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, p.in_dtype);
-                                        const float cand =
-                                            meta->beta[x] * (vx - meta->alpha[x] * v[C::V >= C::LPR ? x % C::NVL : 0]);
-                                        const float wx = __shfl_sync(FULL_MASK, cand, gbase + opos);
-                                        if (pg == 0) p.ring_rec[(unit_ring + (pos0 + x) % L) * rec_floats + 4 + j] = wx;
+                                for (int r = 0; r < 2; ++r)
 #pragma unroll
-                                        for (int i = 0; i < C::NVL; ++i)
-                                            v[i] = fmaf(coef[(cpr + x) * C::V + held(i)], wx, v[i]);
-                                    }
-                                }
-                                if (pg % C::DUP == 0) {
-#pragma unroll
-                                    for (int i = 0; i < C::NVL; ++i) {
-                                        const int idx = held(i);
-                                        if (idx >= TMAX && idx - TMAX < T)
-                                            store_elem(p.out, (((int64_t)b * T + (idx - TMAX)) * p.Hv + h) * p.dv + j,
-                                                       p.out_dtype, v[i]);
-                                    }
-                                }
+                                    for (int i = 0; i < C::NVL; ++i)
+                                        sums[((q + r) * C::RPP + rsub) * (C::V + 1) + held(i)] = v[r][i];
                             }
                         }
                         if (!ok) break;
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&cempty[cs]);
+                        if (lane == 0) mbar_arrive_n(&cempty[cs], fold ? 1 : C::SUB);
+                        if (!have_coef && !(ok = mbar_wait(&cready[hs], hph))) break;  // the window's coefficients
+                        have_coef = true;
+                        if (lane < np * C::RPP) {
+                            const int j = j0 + ps0 * C::RPP + lane;
+                            float y[TMAX], z[TMAX];
+#pragma unroll
+                            for (int t = 0; t < TMAX; ++t)
+                                y[t] = sums[lane * (C::V + 1) + t], z[t] = sums[lane * (C::V + 1) + TMAX + t];
+                            // w_x, then its terms into the later sums of the row (the table holds
+                            // zeros where an entry does not precede a token)
+#pragma unroll
+                            for (int x = 0; x < TMAX; ++x) {
+                                if (x < T) {
+                                    const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, p.in_dtype);
+                                    const float wx = meta->beta[x] * (vx - meta->alpha[x] * y[x]);
+                                    p.ring_rec[(unit_ring + (pos0 + x) % L) * rec_floats + 4 + j] = wx;
+                                    const float* cx = coef + (cpr + x) * C::V;
+#pragma unroll
+                                    for (int t = 0; t < TMAX; ++t)
+                                        y[t] = fmaf(cx[t], wx, y[t]), z[t] = fmaf(cx[TMAX + t], wx, z[t]);
+                                }
+                            }
+#pragma unroll
+                            for (int t = 0; t < TMAX; ++t)
+                                if (t < T)
+                                    store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, z[t]);
+                        }
+                        __syncwarp();  // the tile is free for the next item
                     }
                 }
                 if (!ok) break;
