@@ -36,6 +36,8 @@ def lib() -> C.CDLL:
             "orc_l2norm": (None, [I, P, D, P]),
             "orc_decode_head": (None, [I, I, P, I, P, P, P, I, D, D, P]),
             "orc_decode_step": (I, [I, I, I, I, I, I64, P, I, P, P, P, P, P, P, I, P, P, P, I]),
+            "orc_spec_head": (None, [I, I, I, P, I, P, P, P, P, P, I, P, P, P]),
+            "orc_spec_step": (I, [I, I, I, I, I, I, I64, P, I, P, P, P, P, P, P, P, I, P, P, P, I]),
             "orc_replay_window": (I, [I, I, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
             "orc_replay_flush": (I, [I, I, I, P, I, P, P, I, P, P, P, I]),
             "orc_replay_rollback": (I, [P, I, I]),
@@ -125,6 +127,50 @@ def decode_step(pool: np.ndarray, sdt, slots, q, k, v, a, b, idt, A_log, dt_bias
     bad = lib().orc_decode_step(B, Hk, Hv, dk, dv, num_slots, _ptr(pool), _code(sdt), _ptr(slots),
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(idt),
                                 _ptr(A_log), _ptr(dt_bias), _ptr(out), int(nthreads))
+    return out, bad
+
+
+# ---------------------------------------------------------------- speculative step
+
+
+def spec_head(S: np.ndarray, sdt, q, k, v, idt, alpha, beta, write=None) -> tuple[np.ndarray, np.ndarray]:
+    """One head's speculative step over a T-token window from the state S ([dv, dk] storage array,
+    not modified): q, k [T, dk] and v [T, dv] in idt, gates alpha, beta [T]. Returns (out [T, dv]
+    fp64, copies [T, dv, dk] in sdt: the state after each token, rounded once; rows where write is
+    False are left zero)."""
+    assert S.dtype == NPTYPE[_code(sdt)] and S.flags["C_CONTIGUOUS"]
+    dv, dk = S.shape
+    q, k, v = _arr(q, idt), _arr(k, idt), _arr(v, idt)
+    T = q.shape[0]
+    alpha = np.ascontiguousarray(alpha, dtype=np.float64)
+    beta = np.ascontiguousarray(beta, dtype=np.float64)
+    write = np.ones(T, np.int32) if write is None else np.ascontiguousarray(write, dtype=np.int32)
+    out = np.empty((T, dv), dtype=np.float64)
+    copies = np.zeros((T, dv, dk), dtype=S.dtype)
+    lib().orc_spec_head(dk, dv, T, _ptr(S), _code(sdt), _ptr(copies), _ptr(write), _ptr(q), _ptr(k), _ptr(v),
+                        _code(idt), _ptr(alpha), _ptr(beta), _ptr(out))
+    return out, copies
+
+
+def spec_step(pool: np.ndarray, sdt, src_slots, dst_slots, q, k, v, a, b, idt, A_log, dt_bias,
+              nthreads: int = 1) -> tuple[np.ndarray, int]:
+    """Speculative step of a batch with one state copy per window token: pool [num_slots, Hv, dv,
+    dk] is updated in place; src_slots [B], dst_slots [B, T] (< 0: no copy); q, k [B, T, Hk, dk],
+    v [B, T, Hv, dv], a, b [B, T, Hv]. Returns (out [B, T, Hv, dv] fp64, number of units with an
+    out-of-range slot)."""
+    assert pool.dtype == NPTYPE[_code(sdt)] and pool.flags["C_CONTIGUOUS"]
+    num_slots, Hv, dv, dk = pool.shape
+    q, k, v, a, b = (_arr(x, idt) for x in (q, k, v, a, b))
+    src_slots = np.ascontiguousarray(src_slots, dtype=np.int32)
+    dst_slots = np.ascontiguousarray(dst_slots, dtype=np.int32)
+    B, T = dst_slots.shape
+    Hk = q.size // (B * T * dk)
+    A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+    dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+    out = np.empty((B, T, Hv, dv), dtype=np.float64)
+    bad = lib().orc_spec_step(B, T, Hk, Hv, dk, dv, num_slots, _ptr(pool), _code(sdt), _ptr(src_slots),
+                              _ptr(dst_slots), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(idt),
+                              _ptr(A_log), _ptr(dt_bias), _ptr(out), int(nthreads))
     return out, bad
 
 

@@ -241,6 +241,93 @@ int orc_decode_step(int B, int Hk, int Hv, int dk, int dv, int64_t num_slots, vo
     return bad;
 }
 
+/* ------------------------------------------------------------------ speculative step */
+
+/* The window's tokens applied in order to the state, each a plain decode step;
+ * the copy after token t is the state rounded once, while the recursion goes on
+ * from the unrounded state. */
+void orc_spec_head(int dk, int dv, int T, const void* S_in, int sdt, void* S_out, const int32_t* write,
+                   const void* q, const void* k, const void* v, int idt, const double* alpha,
+                   const double* beta, double* out) {
+    int64_t n = (int64_t)dk * dv;
+    double* Sd = (double*)malloc(sizeof(double) * (size_t)n);
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * dk + dv));
+    double *kr = buf, *qr = buf + dk, *kn = buf + 2 * dk, *qn = buf + 3 * dk, *vv = buf + 4 * dk;
+    load_vec(S_in, 0, (int)n, sdt, Sd);
+    for (int t = 0; t < T; ++t) {
+        load_vec(k, (int64_t)t * dk, dk, idt, kr);
+        load_vec(q, (int64_t)t * dk, dk, idt, qr);
+        load_vec(v, (int64_t)t * dv, dv, idt, vv);
+        orc_l2norm(dk, kr, 1.0, kn);
+        orc_l2norm(dk, qr, 1.0 / sqrt((double)dk), qn);
+        rule_step(dk, dv, Sd, kn, vv, alpha[t], beta[t]);
+        readout(dk, dv, Sd, qn, out + (int64_t)t * dv);
+        if (write[t])
+            for (int64_t i = 0; i < n; ++i) orc_store(S_out, (int64_t)t * n + i, sdt, Sd[i]);
+    }
+    free(buf);
+    free(Sd);
+}
+
+int orc_spec_step(int B, int T, int Hk, int Hv, int dk, int dv, int64_t num_slots, void* pool, int sdt,
+                  const int32_t* src_slots, const int32_t* dst_slots, const void* q, const void* k,
+                  const void* v, const void* a, const void* b, int idt, const float* A_log,
+                  const float* dt_bias, double* out, int nthreads) {
+    int bad = 0;
+    int group = Hv / Hk;
+    int64_t units = (int64_t)B * Hv, n = (int64_t)dk * dv;
+    int esz = orc_dtype_size(sdt);
+    (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 4) reduction(+ : bad) num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h / group;
+        int32_t src = src_slots[bi];
+        int ok = src >= 0 && src < num_slots;
+        for (int t = 0; t < T; ++t) {
+            int32_t d = dst_slots[(int64_t)bi * T + t];
+            if (d >= num_slots) ok = 0;
+        }
+        if (!ok) {
+            if (src >= 0) bad += 1; /* the source or a destination out of range */
+            for (int t = 0; t < T; ++t)
+                for (int j = 0; j < dv; ++j) out[(((int64_t)bi * T + t) * Hv + h) * dv + j] = 0.0;
+            continue;
+        }
+        double* al = (double*)malloc(sizeof(double) * (size_t)(2 * T));
+        double* be = al + T;
+        int32_t* wr = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+        double* o = (double*)malloc(sizeof(double) * (size_t)(T * dv));
+        char* qs = (char*)malloc((size_t)(2 * T * dk + T * dv) * (size_t)orc_dtype_size(idt));
+        char *ks = qs + (size_t)T * dk * orc_dtype_size(idt), *vs = ks + (size_t)T * dk * orc_dtype_size(idt);
+        void* copies = malloc((size_t)(T * n) * (size_t)esz);
+        int isz = orc_dtype_size(idt);
+        for (int t = 0; t < T; ++t) {
+            int64_t g = ((int64_t)bi * T + t) * Hv + h;
+            orc_gating(A_log[h], dt_bias[h], orc_load(a, g, idt), orc_load(b, g, idt), &al[t], &be[t]);
+            wr[t] = dst_slots[(int64_t)bi * T + t] >= 0;
+            memcpy(qs + (size_t)t * dk * isz, elem_ptr(q, (((int64_t)bi * T + t) * Hk + kh) * dk, idt), (size_t)dk * isz);
+            memcpy(ks + (size_t)t * dk * isz, elem_ptr(k, (((int64_t)bi * T + t) * Hk + kh) * dk, idt), (size_t)dk * isz);
+            memcpy(vs + (size_t)t * dv * isz, elem_ptr(v, g * dv, idt), (size_t)dv * isz);
+        }
+        orc_spec_head(dk, dv, T, (const char*)pool + ((int64_t)src * Hv + h) * n * esz, sdt, copies, wr, qs, ks,
+                      vs, idt, al, be, o);
+        for (int t = 0; t < T; ++t) {
+            for (int j = 0; j < dv; ++j) out[(((int64_t)bi * T + t) * Hv + h) * dv + j] = o[(int64_t)t * dv + j];
+            if (wr[t])
+                memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T + t] * Hv + h) * n * esz,
+                       (const char*)copies + (size_t)t * n * esz, (size_t)n * esz);
+        }
+        free(copies);
+        free(qs);
+        free(o);
+        free(wr);
+        free(al);
+    }
+    return bad;
+}
+
 /* ------------------------------------------------------------------ ReplaySSM */
 
 /* The fp64 state after the first n buffered entries, rebuilt from S0 by

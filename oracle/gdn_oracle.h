@@ -53,6 +53,27 @@ int orc_decode_step(int B, int Hk, int Hv, int dk, int dv, int64_t num_slots, vo
                     const void* b, int idt, const float* A_log, const float* dt_bias, double* out,
                     int nthreads);
 
+/* Speculative step with one state copy per window token -- the baseline a
+ * ReplaySSM verify window replaces. One (sequence, value head): the fp64
+ * state loaded from S_in (dv*dk elements of sdt) takes the T window tokens in
+ * order (q, k [T][dk], v [T][dv] in idt; gates alpha, beta [T]); after token
+ * t the state is rounded into S_out + t*dv*dk when write[t] != 0, and the
+ * recursion continues from the unrounded state; out[t*dv + j] = o_t. */
+void orc_spec_head(int dk, int dv, int T, const void* S_in, int sdt, void* S_out, const int32_t* write,
+                   const void* q, const void* k, const void* v, int idt, const double* alpha,
+                   const double* beta, double* out);
+
+/* The same for a batch through slot indices: sequence b starts from
+ * pool[src_slots[b]] and writes its state after window token t to
+ * pool[dst_slots[b*T + t]] (skipped when < 0). Activations are q, k
+ * [B][T][Hk][dk], v [B][T][Hv][dv], a, b [B][T][Hv]; out [B][T][Hv][dv]. Every
+ * source is read before any copy is written. src < 0 is padding (outputs zero,
+ * nothing written). Returns the number of units with a slot >= num_slots. */
+int orc_spec_step(int B, int T, int Hk, int Hv, int dk, int dv, int64_t num_slots, void* pool, int sdt,
+                  const int32_t* src_slots, const int32_t* dst_slots, const void* q, const void* k,
+                  const void* v, const void* a, const void* b, int idt, const float* A_log,
+                  const float* dt_bias, double* out, int nthreads);
+
 /* ReplaySSM, one (sequence, value head). The replay state is the checkpoint
  * S0 (dv*dk elements of sdt), the inputs of the entries buffered since the
  * checkpoint in arrival order -- raw k [L][dk] and v [L][dv] in idt, gates
