@@ -158,6 +158,45 @@ int gdn_decode_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype,
     return launched(gdn::dispatch_decode(state_dtype, dims->dk, p, static_cast<cudaStream_t>(stream)), fn);
 }
 
+int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* src_slots,
+                  const int32_t* dst_slots, int32_t T, const void* q, const void* k, const void* v, const void* a,
+                  const void* b, int32_t in_dtype, const float* A_log, const float* dt_bias, void* out,
+                  int32_t out_dtype, int32_t* dev_err, void* stream) {
+    const char* fn = "gdn_spec_step";
+    int rc = check_dims(dims, fn);
+    if (rc) return rc;
+    if (T < 1 || T > gdn::SPEC_WINDOW_MAX) return fail(GDN_ERR_WINDOW, "%s: T=%d not in [1, 8]", fn, T);
+    if (dims->B == 0) return GDN_OK;
+    if (!state_pool || !src_slots || !dst_slots || !dev_err)
+        return fail(GDN_ERR_NULL, "%s: state_pool, src_slots, dst_slots or dev_err is NULL", fn);
+    if (!dtype_ok(state_dtype)) return fail(GDN_ERR_DTYPE, "%s: unsupported state dtype %d", fn, state_dtype);
+    rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
+    if (rc) return rc;
+    if (!aligned16(state_pool) || !aligned_to(src_slots, 4) || !aligned_to(dst_slots, 4) || !aligned_to(dev_err, 4))
+        return fail(GDN_ERR_ALIGN, "%s: state_pool must be 16-byte aligned", fn);
+    gdn::SpecArgs p{};
+    p.pool = state_pool, p.src_slots = src_slots, p.dst_slots = dst_slots;
+    p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias;
+    p.out = out, p.dev_err = dev_err;
+    p.num_slots = dims->num_slots;
+    p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.T = T;
+    p.in_dtype = in_dtype, p.out_dtype = out_dtype;
+    p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
+    chunking(dims->dk, dims->dv, gdn::dtype_size(state_dtype), p.rows, p.nchunk);
+    const int tmax = T <= 4 ? 4 : 8;
+    bool too_big = false;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (state_dtype == GDN_F32)
+        e = gdn::dispatch_spec_f32(dims->dk, tmax, p, s, too_big);
+    else if (state_dtype == GDN_BF16)
+        e = gdn::dispatch_spec_bf16(dims->dk, tmax, p, s, too_big);
+    else
+        e = gdn::dispatch_spec_f16(dims->dk, tmax, p, s, too_big);
+    if (too_big) return fail(GDN_ERR_SHAPE, "%s: T=%d, dv=%d do not fit in shared memory", fn, T, dims->dv);
+    return launched(e, fn);
+}
+
 int gdn_replay_step(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* q,
                     const void* k, const void* v, const void* a, const void* b, int32_t in_dtype, const float* A_log,
                     const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {

@@ -7,6 +7,7 @@
 
 #include "gdn_decode.cuh"
 #include "gdn_replay.cuh"
+#include "gdn_spec.cuh"
 
 namespace gdn {
 
@@ -17,6 +18,11 @@ cudaError_t dispatch_decode(int state_dtype, int dk, const DecodeArgs& a, cudaSt
 cudaError_t dispatch_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_replay_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+
+// tmax in {4, 8}. too_big is set when the layout does not fit in shared memory.
+cudaError_t dispatch_spec_f32(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_spec_bf16(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_spec_f16(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
 
 cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
                             int B, int Hv, int T, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);

@@ -1,0 +1,11 @@
+// Instantiations of the speculative-step kernel for bf16 states (dk x window size).
+#include "gdn_dispatch.h"
+#include "gdn_launch_spec.cuh"
+
+namespace gdn {
+
+cudaError_t dispatch_spec_bf16(int dk, int tmax, SpecArgs& a, cudaStream_t s, bool& too_big) {
+    return dispatch_spec_t<__nv_bfloat16>(dk, tmax, a, s, too_big);
+}
+
+}  // namespace gdn

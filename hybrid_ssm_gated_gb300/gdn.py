@@ -46,6 +46,7 @@ _P = C.c_void_p
 _I = C.c_int32
 _SIGS = {
     "gdn_decode_step": [C.POINTER(gdn_dims), _P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P],
+    "gdn_spec_step": [C.POINTER(gdn_dims), _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P],
     "gdn_replay_step": [C.POINTER(gdn_dims), C.POINTER(gdn_replay_cache), _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                         _I, _P, _P],
     "gdn_verify_window": [C.POINTER(gdn_dims), C.POINTER(gdn_replay_cache), _P, _I, _P, _P, _P, _P, _P, _I, _P, _P,
@@ -128,6 +129,19 @@ def gdn_decode_step(state_pool, slots, q, k, v, a, b, A_log, dt_bias, out, dev_e
     _check(lib().gdn_decode_step(C.byref(d), _ptr(state_pool), _code(state_pool), _ptr(slots), _ptr(q), _ptr(k),
                                  _ptr(v), _ptr(a), _ptr(b), _code(q), _ptr(A_log), _ptr(dt_bias), _ptr(out),
                                  _code(out), _ptr(dev_err), _stream(stream)))
+
+
+def gdn_spec_step(state_pool, src_slots, dst_slots, q, k, v, a, b, A_log, dt_bias, out, dev_err,
+                  stream=None) -> None:
+    """Speculative step with one state copy per window token: state_pool [num_slots, Hv, dv, dk];
+    src_slots [B] int32; dst_slots [B, T] int32; q, k [B, T, Hk, dk]; v [B, T, Hv, dv];
+    a, b [B, T, Hv]; A_log, dt_bias [Hv] fp32; out [B, T, Hv, dv]; dev_err [1] int32."""
+    num_slots, Hv, dv, dk = state_pool.shape
+    B, T = dst_slots.shape
+    d = make_dims(B, q.shape[-2], Hv, dk, dv, num_slots)
+    _check(lib().gdn_spec_step(C.byref(d), _ptr(state_pool), _code(state_pool), _ptr(src_slots), _ptr(dst_slots),
+                               int(T), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(q), _ptr(A_log),
+                               _ptr(dt_bias), _ptr(out), _code(out), _ptr(dev_err), _stream(stream)))
 
 
 class ReplayCache:

@@ -62,7 +62,7 @@ extern "C" {
 #define GDN_ERR_NULL (-1)    /* a required pointer is NULL */
 #define GDN_ERR_DTYPE (-2)   /* unsupported dtype or dtype mismatch */
 #define GDN_ERR_SHAPE (-3)   /* unsupported dk/dv, Hv % Hk != 0, negative sizes */
-#define GDN_ERR_WINDOW (-4)  /* T < 1, T > L, T > 8, L > 32 */
+#define GDN_ERR_WINDOW (-4)  /* T < 1, T > 8, T > L, L > 32 */
 #define GDN_ERR_ALIGN (-5)   /* a pointer is not 16-byte aligned */
 #define GDN_ERR_LAUNCH (-6)  /* CUDA reported an error at launch */
 
@@ -104,6 +104,34 @@ int gdn_decode_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype,
                     const void* a, const void* b, int32_t in_dtype, const float* A_log,
                     const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err,
                     void* stream);
+
+/*
+ * gdn_spec_step -- speculative step with one state copy per window token: the
+ * baseline that the ReplaySSM verify window replaces (AREX ReplaySSM article,
+ * section "每步写回完整循环状态：SSM 解码的两个瓶颈": to roll back rejected
+ * drafts, the existing implementation keeps a recurrent state per draft token,
+ * about (1 + num_spec) times the state memory).
+ * Sequence b takes a window of T tokens (the last verified token and T-1
+ * drafts, 1 <= T <= 8) from the state in state_pool[src_slots[b]]. After
+ * window token t its state is rounded (round-to-nearest-even) into
+ * state_pool[dst_slots[b*T + t]]; the recursion continues from the unrounded
+ * FP32 state. Output t is o_t = S_t^T q_t. After verification the state of
+ * the last accepted token is the copy in its destination slot.
+ * state_pool  as for gdn_decode_step.
+ * src_slots   [B] int32 (< 0: padding; outputs zero, nothing written).
+ * dst_slots   [B][T] int32 (< 0: that token's copy is not written).
+ *             Preconditions (not checked): no slot appears twice in a call,
+ *             except that a sequence's destinations may include its own
+ *             source slot. A source or destination >= num_slots sets
+ *             GDN_DEVERR_SLOT; that sequence's outputs are zeroed and nothing
+ *             of it is written.
+ * q, k  [B][T][Hk][dk];  v [B][T][Hv][dv];  a, b [B][T][Hv];  out [B][T][Hv][dv].
+ * Errors as gdn_decode_step; T outside [1, 8] gives GDN_ERR_WINDOW.
+ */
+int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* src_slots,
+                  const int32_t* dst_slots, int32_t T, const void* q, const void* k, const void* v,
+                  const void* a, const void* b, int32_t in_dtype, const float* A_log,
+                  const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream);
 
 /*
  * ReplaySSM cache (AREX ReplaySSM article, "缓存输入而非状态"). Everything is

@@ -128,3 +128,22 @@ def test_binding_refuses_host_tensors(lib):
     t = torch.zeros(4)
     with pytest.raises(ValueError):
         gdn._ptr(t)
+
+
+def _spec(lib, dims, T=4, pool=FAKE, sdt=0, src=FAKE, dst=FAKE, q=FAKE, idt=1, err=FAKE):
+    return lib.gdn_spec_step(C.byref(dims), pool, sdt, src, dst, T, q, FAKE, FAKE, FAKE, FAKE, idt, FAKE, FAKE,
+                             FAKE, 0, err, None)
+
+
+def test_spec_rejections(lib):
+    d = _dims()
+    assert _spec(lib, d, T=0) == -4  # GDN_ERR_WINDOW
+    assert _spec(lib, d, T=9) == -4
+    assert _spec(lib, _dims(dk=96)) == -3
+    assert _spec(lib, d, dst=None) == -1
+    assert _spec(lib, d, err=None) == -1
+    assert _spec(lib, d, sdt=4) == -2
+    assert _spec(lib, d, idt=5) == -2
+    assert _spec(lib, d, pool=FAKE + 8) == -5
+    assert _spec(lib, d, q=FAKE + 4) == -5
+    assert _spec(lib, _dims(B=0), pool=None, src=None, dst=None) == 0  # nothing to do, nothing touched
