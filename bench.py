@@ -61,6 +61,15 @@ def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes:
             T * DV * out_bytes + 16 + (state if fold else 0))
 
 
+def spec_bytes_per_seq(T: int, state_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+    """Algorithmic bytes of one speculative step with one state copy per window token, one
+    sequence (all heads): the source state read, T state copies written, T tokens of inputs,
+    T outputs, T + 1 slot indices."""
+    state = HV * DK * DV * state_bytes
+    return (state * (1 + T) + T * (2 * HK * DK * in_bytes + HV * DV * in_bytes + 2 * HV * in_bytes) +
+            T * HV * DV * out_bytes + 4 * (1 + T))
+
+
 # ------------------------------------------------------------------ helpers
 
 
@@ -358,14 +367,45 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             gdn.gdn_rollback(cache, slots, acc, T, err, stream)
 
         vrounds = max(16, args.steps // 40)
+        torch.cuda.synchronize()
+        cv = (cache.pos - cache.ckpt_pos)[slots.long(), 0].cpu().numpy().astype(np.int64)
+        acc_np = acc.cpu().numpy().astype(np.int64)
         el, lm = timed(vround, vrounds, 3)
+        vbytes = 0
+        for _ in range(3 + vrounds):  # host replay of the counts through warm-up and timed rounds
+            fold = cv + T > L_RING
+            vbytes_round = HV * sum(replay_unit_bytes(int(x), T, bool(f), cs) for x, f in zip(cv, fold))
+            cv = np.where(fold, 0, cv) + 1 + acc_np
+            vbytes = vbytes_round  # bytes of the last round (the counts cycle; rounds differ little)
         accepted_tokens = float((acc.float() + 1).sum().item())
+        vgbs = vbytes / (el / vrounds / 1e3) / 1e9
         modes[f"verify_T4_{ckname}_ckpt"] = {
             "window_tokens_per_s": world * B * T * vrounds / (el / 1e3),
             "accepted_tokens_per_s": world * accepted_tokens * vrounds / (el / 1e3),
-            "us_per_round": el / vrounds * 1e3, "T": T, "L": L_RING}
+            "us_per_round": el / vrounds * 1e3, "T": T, "L": L_RING, "hbm_gbs": vgbs, "frac": vgbs / peak,
+            "bytes_per_round": vbytes}
         result["gpu_launches"] += 2 * vrounds
         del cache
+    # the baseline the verify window replaces: T=4 window with one state copy per token
+    T = T_VERIFY
+    perm = torch.randperm(B * (T + 1), generator=gen, device=dev).to(torch.int32)
+    ssrc, sdst = perm[:B].contiguous(), perm[B:].reshape(B, T).contiguous()
+    q4, k4 = randn(B, T, HK, DK), randn(B, T, HK, DK)
+    v4, a4, b4 = randn(B, T, HV, DV), randn(B, T, HV), randn(B, T, HV)
+    out4 = torch.empty(B, T, HV, DV, device=dev)
+    for sname, sdt, ss in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        sp = (torch.randn(B * (T + 1), HV, DV, DK, generator=gen, device=dev) * 0.1).to(sdt)
+        srounds = max(16, args.steps // 40)
+        el, lm = timed(lambda: gdn.gdn_spec_step(sp, ssrc, sdst, q4, k4, v4, a4, b4, A_log, dt_bias, out4, err, stream),
+                       srounds, 3)
+        sb = spec_bytes_per_seq(T, ss) * B
+        sgbs = sb / (lm / 1e3) / 1e9
+        modes[f"spec_T4_{sname}_state"] = {
+            "window_tokens_per_s": world * B * T * srounds / (el / 1e3), "us_per_round": el / srounds * 1e3,
+            "T": T, "hbm_gbs": sgbs, "frac": sgbs / peak, "bytes_per_round": sb,
+            "state_write_bytes_per_window_token": HV * DK * DV * ss}
+        result["gpu_launches"] += srounds
+        del sp
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during the mode runs")
     result["modes"] = modes
@@ -435,6 +475,7 @@ def run_case(args) -> None:
     decode:  B sequences, fp32/bf16/fp16 state pool of 2B slots.
     replay:  ReplaySSM steps, L=16 ring pre-filled to start offsets in [0, 15].
     verify:  T=4 verify windows + rollbacks on the same cache.
+    spec:    T=4 speculative steps with one state copy per window token, pool of 5B slots.
     """
     import numpy as np
     import torch
@@ -458,6 +499,15 @@ def run_case(args) -> None:
         out = torch.empty(Bc, HV, DV, device=dev)
         for _ in range(args.steps):
             gdn.gdn_decode_step(pool, slots, q, k, v, a, b, A_log, dt_bias, out, err)
+    elif args.case == "spec":
+        T = T_VERIFY
+        pool = (torch.randn(Bc * (T + 1), HV, DV, DK, generator=g, device=dev) * 0.1).to(sdt)
+        perm = torch.randperm(Bc * (T + 1), generator=g, device=dev).to(torch.int32)
+        src, dst = perm[:Bc].contiguous(), perm[Bc:].reshape(Bc, T).contiguous()
+        q, k, v, a, b = rnd(Bc, T, HK, DK), rnd(Bc, T, HK, DK), rnd(Bc, T, HV, DV), rnd(Bc, T, HV), rnd(Bc, T, HV)
+        out = torch.empty(Bc, T, HV, DV, device=dev)
+        for _ in range(args.steps):
+            gdn.gdn_spec_step(pool, src, dst, q, k, v, a, b, A_log, dt_bias, out, err)
     else:
         T = T_VERIFY if args.case == "verify" else 1
         cache = gdn.ReplayCache.allocate(2 * Bc, HV, DK, DV, L_RING, sdt, torch.bfloat16, device=dev)
@@ -489,7 +539,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "replay", "verify"],
+    ap.add_argument("--case", choices=["decode", "replay", "verify", "spec"],
                     help="run --steps untimed launches of one kernel for a profiler and exit")
     ap.add_argument("--B", type=int, default=B, help="batch of --case")
     ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16", "f16"], help="state dtype of --case")
