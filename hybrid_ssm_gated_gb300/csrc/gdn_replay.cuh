@@ -97,6 +97,11 @@ struct ReplayArgs {
 
 constexpr int REPLAY_META = 128;  // bytes of per-unit metadata at the start of a head stage
 
+#ifndef GDN_REPLAY_CREW_PASSES
+#define GDN_REPLAY_CREW_PASSES 4
+#endif
+constexpr int REPLAY_CREW_PASSES = GDN_REPLAY_CREW_PASSES;  // coefficient passes per crew warp
+
 template <typename ST, int DK, int TMAX, int NCW>
 struct ReplayCfg {
     static constexpr int VEC = Store<ST>::VEC;
@@ -429,12 +434,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
         const int dbase = (base + nitems) % NCW;  // warp of the unit's first coefficient pass
         const int i0 = (cw - base + NCW) % NCW;   // this warp's first item
         const int d0 = (cw - dbase + NCW) % NCW;  // this warp's first coefficient pass
-        // the crew: warps with coefficient passes, at least the appender; its last warp to finish
+        // the crew: warps with coefficient passes (up to REPLAY_CREW_PASSES each, so that few warps
+        // spend a window normalisation on them), at least the appender; its last warp to finish
         // arms the table barrier, so row warps never wait for warps busy with other units
-        const int crew = max(1, min(NCW, (J + C::RPP - 1) / C::RPP));
+        const int dpasses = (J + C::RPP - 1) / C::RPP;
+        const int crew = max(1, min(NCW, (dpasses + REPLAY_CREW_PASSES - 1) / REPLAY_CREW_PASSES));
         const bool rows_here = i0 < nitems;
         const bool in_crew = d0 < crew;
-        const bool dots_here = d0 * C::RPP < J;
+        const bool dots_here = in_crew && J > 0;
         const bool appender = d0 == 0;
         if (rows_here || in_crew) {
             const int b = unit / p.Hv, h = unit - b * p.Hv;
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // token t: coef[x][t] = (k_x.k_t) times the decay from x to token t's S^T k_t,
                 // coef[x][TMAX + t] = (k_x.q_t) times the decay from x to token t's output; zero where
                 // the entry does not precede the token
-                for (int dp = d0; dp * C::RPP < J; dp += NCW) {
+                for (int dp = d0; dp < dpasses; dp += crew) {
                     const int x = dp * C::RPP + rsub;
                     const int xc = min(x, J - 1);
                     const bool ring = xc < cpr;
@@ -762,9 +769,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                             p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                         }
                     } else {
-                        // Passes of RPP rows: the 2T sums of a row are reduce-scattered over its
-                        // lanes and parked in this warp's tile, one tile row per state row; then one
-                        // lane per row runs the window's recursion and stores the row's outputs.
+                        // Passes of RPP rows: the 2T sums of S0 with the window's keys and queries
+                        // are reduce-scattered over a row's lanes and parked in this warp's tile, one
+                        // tile row per state row; then one lane per row adds the buffered entries'
+                        // terms, runs the window's recursion and stores the row's outputs. The
+                        // coefficient table is needed only then.
                         const int np = fold ? C::FP : C::PPI;                    // passes of this (sub-)item
                         const int ps0 = fold ? (it - bi * C::SUB) * C::FP : 0;  // its first pass
                         // two passes at a time (np is even): their loads, FMA chains and shuffles interleave
@@ -796,23 +805,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 }
                                 G1 = G2;
                             }
-                            if (cpr > 0) {
-                                if (!have_coef && !(ok = mbar_wait(&cready[hs], hph))) break;
-                                have_coef = true;
-                                // ring terms, split over the row's lanes before the reduction
-                                for (int f = pg; f < cpr; f += C::LPR) {
-                                    const float w0 = rec[f * rec_floats + 4 + jr[0]];
-                                    const float w1 = rec[f * rec_floats + 4 + jr[1]];
-#pragma unroll
-                                    for (int i = 0; i < C::V; i += 4) {
-                                        const float4 c4 = *reinterpret_cast<const float4*>(coef + f * C::V + i);
-                                        v[0][i] = fmaf(c4.x, w0, v[0][i]), v[0][i + 1] = fmaf(c4.y, w0, v[0][i + 1]);
-                                        v[0][i + 2] = fmaf(c4.z, w0, v[0][i + 2]), v[0][i + 3] = fmaf(c4.w, w0, v[0][i + 3]);
-                                        v[1][i] = fmaf(c4.x, w1, v[1][i]), v[1][i + 1] = fmaf(c4.y, w1, v[1][i + 1]);
-                                        v[1][i + 2] = fmaf(c4.z, w1, v[1][i + 2]), v[1][i + 3] = fmaf(c4.w, w1, v[1][i + 3]);
-                                    }
-                                }
-                            }
                             reduce_scatter_values<C::V, C::LPR>(v[0], pg);
                             reduce_scatter_values<C::V, C::LPR>(v[1], pg);
                             if (pg % C::DUP == 0) {
@@ -834,24 +826,36 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
 #pragma unroll
                             for (int t = 0; t < TMAX; ++t)
                                 y[t] = sums[lane * (C::V + 1) + t], z[t] = sums[lane * (C::V + 1) + TMAX + t];
+                            // the buffered entries' terms (coefficients broadcast from the table)
+                            for (int f = 0; f < cpr; ++f) {
+                                const float wf = rec[f * rec_floats + 4 + j];
+                                const float* cf = coef + f * C::V;
+#pragma unroll
+                                for (int t = 0; t < TMAX; ++t)
+                                    y[t] = fmaf(cf[t], wf, y[t]), z[t] = fmaf(cf[TMAX + t], wf, z[t]);
+                            }
                             // w_x, then its terms into the later sums of the row (the table holds
                             // zeros where an entry does not precede a token)
+                            int ri = pos0 % L;  // ring index of window token x (advanced without a division)
+                            float* wcol = p.ring_rec + unit_ring * rec_floats + 4 + j;
 #pragma unroll
                             for (int x = 0; x < TMAX; ++x) {
                                 if (x < T) {
                                     const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, p.in_dtype);
                                     const float wx = meta->beta[x] * (vx - meta->alpha[x] * y[x]);
-                                    p.ring_rec[(unit_ring + (pos0 + x) % L) * rec_floats + 4 + j] = wx;
+                                    wcol[(int64_t)ri * rec_floats] = wx;
+                                    if (++ri == L) ri = 0;
                                     const float* cx = coef + (cpr + x) * C::V;
 #pragma unroll
                                     for (int t = 0; t < TMAX; ++t)
                                         y[t] = fmaf(cx[t], wx, y[t]), z[t] = fmaf(cx[TMAX + t], wx, z[t]);
                                 }
                             }
+                            const int64_t ob = ((int64_t)b * T * p.Hv + h) * p.dv + j;  // output (t = 0)
+                            const int64_t ot = (int64_t)p.Hv * p.dv;                    // next token
 #pragma unroll
                             for (int t = 0; t < TMAX; ++t)
-                                if (t < T)
-                                    store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, z[t]);
+                                if (t < T) store_elem(p.out, ob + t * ot, p.out_dtype, z[t]);
                         }
                         __syncwarp();  // the tile is free for the next item
                     }
