@@ -101,6 +101,10 @@ constexpr int REPLAY_META = 128;  // bytes of per-unit metadata at the start of 
 #define GDN_REPLAY_CREW_PASSES 4
 #endif
 constexpr int REPLAY_CREW_PASSES = GDN_REPLAY_CREW_PASSES;  // coefficient passes per crew warp
+#ifndef GDN_REPLAY_WIDE_FOLD_PASSES
+#define GDN_REPLAY_WIDE_FOLD_PASSES 4
+#endif
+constexpr int REPLAY_WIDE_FOLD_PASSES = GDN_REPLAY_WIDE_FOLD_PASSES;  // passes of a fold sub-item, T > 1
 
 template <typename ST, int DK, int TMAX, int NCW>
 struct ReplayCfg {
@@ -119,13 +123,15 @@ struct ReplayCfg {
     static constexpr int NVL = V >= LPR ? V / LPR : 1;  // sums a lane holds after the reduce-scatter
     static constexpr int DUP = V >= LPR ? 1 : LPR / V;  // lanes holding the same sum
     static constexpr int FP = 2;                        // rows a lane folds at once (key reuse)
-    // a fold unit's items are split further (SUB sub-items of FP passes), so that its extra work
-    // spreads over all warps; chunk releases count in sub-items
-    static constexpr int SUB = PPI / FP;
+    // a fold unit's items are split further (SUB sub-items of FPS passes), so that its extra work
+    // spreads over all warps; chunk releases count in sub-items. Wider windows take four passes a
+    // sub-item, so that their per-lane recursion runs on more rows at once.
+    static constexpr int FPS = TMAX == 1 ? FP : (PPI < REPLAY_WIDE_FOLD_PASSES ? PPI : REPLAY_WIDE_FOLD_PASSES);
+    static constexpr int SUB = PPI / FPS;
     static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
     static constexpr int THREADS = (NCW + 1) * 32;
     static_assert(E % VEC == 0 && DK % E == 0 && LPR >= 2 && LPR <= 32, "unsupported dk");
-    static_assert(PPI % FP == 0 && ITEM == 32, "item blocking");
+    static_assert(PPI % FPS == 0 && FPS % FP == 0 && ITEM == 32, "item blocking");
 };
 
 // Per-unit metadata written by the producer at the start of a head stage.
@@ -672,7 +678,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         // with the sums of row pg * RPP + rsub of the item
                         if (fold) {
                             // sub-item: FP passes, folded, then dot products reduced per pass
-                            const int ps0 = (it - bi * C::SUB) * C::FP;
+                            const int ps0 = (it - bi * C::SUB) * C::FPS;
                             float s[C::FP][C::E];
                             int jr[C::FP];
 #pragma unroll
@@ -774,8 +780,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         // tile row per state row; then one lane per row adds the buffered entries'
                         // terms, runs the window's recursion and stores the row's outputs. The
                         // coefficient table is needed only then.
-                        const int np = fold ? C::FP : C::PPI;                    // passes of this (sub-)item
-                        const int ps0 = fold ? (it - bi * C::SUB) * C::FP : 0;  // its first pass
+                        const int np = fold ? C::FPS : C::PPI;                    // passes of this (sub-)item
+                        const int ps0 = fold ? (it - bi * C::SUB) * C::FPS : 0;  // its first pass
                         // two passes at a time (np is even): their loads, FMA chains and shuffles interleave
                         for (int q = 0; q < np; q += 2) {
                             float s2[2][C::E];
