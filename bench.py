@@ -281,7 +281,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         "bytes_per_token": bpt,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps, 6 chunk stages)", "launch_us": launch_ms * 1e3,
+                     "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps in groups of 4, 6 chunk stages)", "launch_us": launch_ms * 1e3,
                      "algorithmic_bytes_per_launch": bpt * B},
         "clocks": clocks,
         "gpu_launches": args.steps,

@@ -14,15 +14,20 @@
 // Kernel shape: persistent CTAs over (sequence, value head) units, one
 // producer warp + NCW consumer warps.
 //  - The producer warp fetches slot indices and gates for 32 units at a time
-//    (one lane per unit), then lane 0 streams each unit's state in 16 KB
-//    chunks into an NS-deep shared-memory ring with bulk copies on the TMA
-//    engine (cp.async.bulk + mbarrier transaction counts), together with the
-//    unit's q/k/v rows into an NH-deep "head" ring.
+//    (one lane per unit), then streams each unit's state in 16 KB chunks
+//    into an NS-deep shared-memory ring with bulk copies on the TMA engine
+//    (cp.async.bulk + mbarrier transaction counts), together with the unit's
+//    q/k/v rows into an NH-deep "head" ring; a unit's copies are spread over
+//    the producer's lanes.
 //  - Consumer warps read the chunk from shared memory (128-bit, conflict
 //    free), do the fused update in FP32 registers, and store the new state
 //    (packed to the storage type) and the output straight to global memory.
 //    A row is covered by LPR = dk/16 lanes holding 16 elements each; the two
 //    row dot products are reduced with log2(LPR) xor-shuffles.
+//  - The consumer warps form groups of UW that take units in turn: a unit's
+//    passes go to one group, so each warp normalises q and k for only its
+//    group's units. Every warp still waits for and releases every chunk in
+//    order, so no parity wait can alias.
 //  - Every wait is bounded (GDN_DEVERR_TIMEOUT, then return).
 #pragma once
 
@@ -50,6 +55,10 @@ struct DecodeArgs {
     float q_scale;
 };
 
+#ifndef GDN_DECODE_UNIT_WARPS
+#define GDN_DECODE_UNIT_WARPS 4
+#endif
+
 constexpr int CHUNK_BYTES = 16384;
 constexpr int DV_MAX = 256;
 
@@ -68,6 +77,11 @@ struct DecodeCfg {
     static constexpr int HEAD = align_up(OFF_V + DV_MAX * 4, 128);
     static constexpr int SMEM = NS * CHUNK_BYTES + NH * HEAD + (2 * NS + 2 * NH) * 8;
     static constexpr int THREADS = (NCW + 1) * 32;
+    // warps per unit: a unit's passes are dealt over UW warps, the NG = NCW / UW groups taking
+    // units in turn
+    static constexpr int UW = GDN_DECODE_UNIT_WARPS < NCW ? GDN_DECODE_UNIT_WARPS : NCW;
+    static constexpr int NG = NCW / UW;
+    static_assert(NCW % UW == 0, "unit warps must divide the consumer warps");
     static_assert(DK % E == 0 && LPR <= 32, "dk must be a multiple of 16 and at most 512");
 };
 
@@ -207,29 +221,39 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
             for (int j = cw * 32 + lane; j < p.dv; j += NCW * 32)
                 store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, 0.f);
         } else {
-            // normalised k and q at this lane's 16 key positions
-            float kn[C::E], qn[C::E];
-#pragma unroll
-            for (int c = 0; c < C::NC; ++c) {
-                const int first = (c * C::LPR + pg) * C::VEC;
-                load_run<C::VEC>(head + C::OFF_K, first, p.in_dtype, kn + c * C::VEC);
-                load_run<C::VEC>(head + C::OFF_Q, first, p.in_dtype, qn + c * C::VEC);
-            }
-            float ssk = 0.f, ssq = 0.f;
-#pragma unroll
-            for (int e = 0; e < C::E; ++e) ssk = fmaf(kn[e], kn[e], ssk), ssq = fmaf(qn[e], qn[e], ssq);
-            ssk = group_sum<C::LPR>(ssk);
-            ssq = group_sum<C::LPR>(ssq);
-            const float ik = rsqrtf(ssk + 1e-6f), iq = rsqrtf(ssq + 1e-6f) * p.q_scale;
-            float qk = 0.f;
-#pragma unroll
-            for (int e = 0; e < C::E; ++e) kn[e] *= ik, qn[e] *= iq, qk = fmaf(kn[e], qn[e], qk);
-            qk = group_sum<C::LPR>(qk);
-            // packed FP32x2 operands: two state elements per instruction
+            // A unit's passes go to one group of UW warps (groups alternate by unit), so each warp
+            // normalises the window for only its group's units; every warp still waits for and
+            // releases every chunk, in order.
+            const bool mine = (n % C::NG) == cw / C::UW;
+            const int gw = cw % C::UW;
+            // normalised k and q at this lane's 16 key positions, in packed FP32x2 pairs
             float2 kn2[C::E / 2], qn2[C::E / 2];
+            float qk = 0.f;
+            if (mine) {
+                float kn[C::E], qn[C::E];
 #pragma unroll
-            for (int e = 0; e < C::E / 2; ++e)
-                kn2[e] = make_float2(kn[2 * e], kn[2 * e + 1]), qn2[e] = make_float2(qn[2 * e], qn[2 * e + 1]);
+                for (int c = 0; c < C::NC; ++c) {
+                    const int first = (c * C::LPR + pg) * C::VEC;
+                    load_run<C::VEC>(head + C::OFF_K, first, p.in_dtype, kn + c * C::VEC);
+                    load_run<C::VEC>(head + C::OFF_Q, first, p.in_dtype, qn + c * C::VEC);
+                }
+                float2 sk = make_float2(0.f, 0.f), sq = sk;
+#pragma unroll
+                for (int e = 0; e < C::E / 2; ++e) {
+                    kn2[e] = make_float2(kn[2 * e], kn[2 * e + 1]), qn2[e] = make_float2(qn[2 * e], qn[2 * e + 1]);
+                    sk = __ffma2_rn(kn2[e], kn2[e], sk), sq = __ffma2_rn(qn2[e], qn2[e], sq);
+                }
+                const float ik = rsqrtf(group_sum<C::LPR>(sk.x + sk.y) + 1e-6f);
+                const float iq = rsqrtf(group_sum<C::LPR>(sq.x + sq.y) + 1e-6f) * p.q_scale;
+                const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
+                float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < C::E / 2; ++e) {
+                    kn2[e] = __fmul2_rn(kn2[e], ik2), qn2[e] = __fmul2_rn(qn2[e], iq2);
+                    d2 = __ffma2_rn(kn2[e], qn2[e], d2);
+                }
+                qk = group_sum<C::LPR>(d2.x + d2.y);
+            }
 
             const int b = unit / p.Hv, h = unit - b * p.Hv;
             char* gstate = static_cast<char*>(p.pool) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
@@ -240,8 +264,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     return;
                 }
                 const unsigned char* tile = chunks + cs * CHUNK_BYTES;
-                // the unit's warp passes are spread over the consumer warps across chunks
-                for (int ps = ((cw - c * passes) % NCW + NCW) % NCW; ps < passes; ps += NCW) {
+                // the unit's warp passes are spread over its group's warps across chunks
+                for (int ps = mine ? ((gw - c * passes) % C::UW + C::UW) % C::UW : passes; ps < passes;
+                     ps += C::UW) {
                     const int r = ps * C::RPP + rsub;
                     const int j = c * p.rows + r;
                     float s[C::E];

@@ -77,18 +77,27 @@ cudaError_t prepare_kernel(Kernel kern, int threads, int smem, int& blocks_per_s
 #ifndef GDN_DECODE_CONSUMER_WARPS
 #define GDN_DECODE_CONSUMER_WARPS 16
 #endif
+// chunk stages for fp32 states and for 16-bit states (measured best: 6 and 8)
 #ifndef GDN_DECODE_CHUNK_STAGES
 #define GDN_DECODE_CHUNK_STAGES 6
+#endif
+#ifndef GDN_DECODE_CHUNK_STAGES_NARROW
+#define GDN_DECODE_CHUNK_STAGES_NARROW 8
 #endif
 #ifndef GDN_DECODE_HEAD_STAGES
 #define GDN_DECODE_HEAD_STAGES 4
 #endif
-constexpr int DEC_NCW = GDN_DECODE_CONSUMER_WARPS, DEC_NS = GDN_DECODE_CHUNK_STAGES, DEC_NH = GDN_DECODE_HEAD_STAGES;
+constexpr int DEC_NCW = GDN_DECODE_CONSUMER_WARPS, DEC_NH = GDN_DECODE_HEAD_STAGES;
+template <typename ST>
+constexpr int decode_stages() {
+    return sizeof(ST) == 4 ? GDN_DECODE_CHUNK_STAGES : GDN_DECODE_CHUNK_STAGES_NARROW;
+}
 
 template <typename ST, int DK>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    using C = DecodeCfg<ST, DK, DEC_NCW, DEC_NS, DEC_NH>;
-    auto kern = decode_kernel<ST, DK, DEC_NCW, DEC_NS, DEC_NH>;
+    constexpr int NS = decode_stages<ST>();
+    using C = DecodeCfg<ST, DK, DEC_NCW, NS, DEC_NH>;
+    auto kern = decode_kernel<ST, DK, DEC_NCW, NS, DEC_NH>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;
