@@ -41,6 +41,8 @@ def lib() -> C.CDLL:
             "orc_replay_window": (I, [I, I, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
             "orc_replay_flush": (I, [I, I, I, P, I, P, P, I, P, P, P, I]),
             "orc_replay_rollback": (I, [P, I, I]),
+            "orc_replay2_window": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
+            "orc_replay2_flush": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(_lib, name)
@@ -184,11 +186,16 @@ class ReplayHead:
     are kept in arrival order (entry e is the e-th token after ckpt_pos):
     raw k [L, dk] and v [L, dv] in the input dtype, alpha/beta [L] fp64.
     meta = [count, pos, ckpt_pos].
+
+    With read_dtype, S0 is a high-precision checkpoint used only for folding and
+    Sr, its copy rounded to read_dtype, is what outputs read (orc_replay2_*).
     """
 
-    def __init__(self, S0: np.ndarray, sdt, idt, L: int, pos: int = 0):
+    def __init__(self, S0: np.ndarray, sdt, idt, L: int, pos: int = 0, read_dtype=None):
         self.sdt, self.idt, self.L = _code(sdt), _code(idt), int(L)
         self.S0 = np.ascontiguousarray(S0, dtype=NPTYPE[self.sdt]).copy()
+        self.rdt = None if read_dtype is None else _code(read_dtype)
+        self.Sr = None if self.rdt is None else round_to(load(self.S0, self.sdt), self.rdt)
         self.dv, self.dk = self.S0.shape
         self.ek = np.zeros((L, self.dk), dtype=NPTYPE[self.idt])
         self.ev = np.zeros((L, self.dv), dtype=NPTYPE[self.idt])
@@ -215,18 +222,29 @@ class ReplayHead:
         a = np.ascontiguousarray(a, dtype=np.float64).reshape(T)
         b = np.ascontiguousarray(b, dtype=np.float64).reshape(T)
         out = np.empty((T, self.dv), dtype=np.float64)
-        rc = lib().orc_replay_window(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
-                                     _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
-                                     _ptr(self.meta), T, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
-                                     float(A_log), float(dt_bias), _ptr(out))
+        if self.rdt is None:
+            rc = lib().orc_replay_window(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
+                                         _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                         _ptr(self.meta), T, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                         float(A_log), float(dt_bias), _ptr(out))
+        else:
+            rc = lib().orc_replay2_window(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.Sr), self.rdt,
+                                          _ptr(self.ek), _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                          _ptr(self.meta), T, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                          float(A_log), float(dt_bias), _ptr(out))
         if rc != 0:
             raise ValueError(f"oracle replay window rejected its input (code {rc})")
         return out
 
     def flush(self, force: bool = True) -> None:
-        rc = lib().orc_replay_flush(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
-                                    _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
-                                    _ptr(self.meta), int(bool(force)))
+        if self.rdt is None:
+            rc = lib().orc_replay_flush(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.ek),
+                                        _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                        _ptr(self.meta), int(bool(force)))
+        else:
+            rc = lib().orc_replay2_flush(self.dk, self.dv, self.L, _ptr(self.S0), self.sdt, _ptr(self.Sr), self.rdt,
+                                         _ptr(self.ek), _ptr(self.ev), self.idt, _ptr(self.ea), _ptr(self.eb),
+                                         _ptr(self.meta), int(bool(force)))
         if rc != 0:
             raise ValueError(f"oracle replay flush rejected its state (code {rc})")
 

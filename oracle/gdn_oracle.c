@@ -391,6 +391,69 @@ int orc_replay_window(int dk, int dv, int L, void* S0, int sdt, void* ek, void* 
     return 0;
 }
 
+/* ------------------------------------------------------------------ ReplaySSM, two checkpoints */
+
+/* A high-precision checkpoint M for the recurrence and a low-precision copy Rd
+ * for reading. Folding: every buffered entry's update is taken from the state
+ * rebuilt from the read copy -- the prediction S^T k, and with it the
+ * correction, come from the copy that every output reads -- and the same
+ * update is applied to the master. Then M is rounded to mdt and Rd is
+ * rewritten as the rounded master, rounded to rdt. With Rd holding the same
+ * values as M this is the single-checkpoint fold. */
+static void fold2(int dk, int dv, void* M, int mdt, void* Rd, int rdt, const void* ek, const void* ev, int idt,
+                  const double* ea, const double* eb, int32_t* meta) {
+    int64_t n = (int64_t)dk * dv;
+    double* Sr = (double*)malloc(sizeof(double) * (size_t)n);
+    double* Sm = (double*)malloc(sizeof(double) * (size_t)n);
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)(2 * dk + dv));
+    double *kr = tmp, *kn = tmp + dk, *vv = tmp + 2 * dk;
+    load_vec(Rd, 0, (int)n, rdt, Sr);
+    load_vec(M, 0, (int)n, mdt, Sm);
+    for (int e = 0; e < meta[0]; ++e) {
+        load_vec(ek, (int64_t)e * dk, dk, idt, kr);
+        load_vec(ev, (int64_t)e * dv, dv, idt, vv);
+        orc_l2norm(dk, kr, 1.0, kn);
+        for (int j = 0; j < dv; ++j) {
+            double* cr = Sr + (int64_t)j * dk;
+            double* cm = Sm + (int64_t)j * dk;
+            double u = 0.0;
+            for (int i = 0; i < dk; ++i) u += cr[i] * kn[i];
+            for (int i = 0; i < dk; ++i) {
+                cr[i] = ea[e] * cr[i] + eb[e] * kn[i] * (vv[j] - ea[e] * u);
+                cm[i] = ea[e] * cm[i] + eb[e] * kn[i] * (vv[j] - ea[e] * u);
+            }
+        }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        double m = orc_round(Sm[i], mdt);
+        orc_store(M, i, mdt, m);
+        orc_store(Rd, i, rdt, m);
+    }
+    free(tmp);
+    free(Sm);
+    free(Sr);
+    meta[0] = 0;
+    meta[2] = meta[1];
+}
+
+int orc_replay2_window(int dk, int dv, int L, void* M, int mdt, void* Rd, int rdt, void* ek, void* ev, int idt,
+                       double* ealpha, double* ebeta, int32_t* meta, int T, const void* q, const void* k,
+                       const void* v, const double* a, const double* b, double A_log, double dt_bias, double* out) {
+    if (T < 1 || T > L) return -1;
+    if (meta[0] < 0 || meta[0] > L || meta[1] - meta[2] != meta[0]) return -2;
+    if (meta[0] + T > L) fold2(dk, dv, M, mdt, Rd, rdt, ek, ev, idt, ealpha, ebeta, meta);
+    /* outputs read the copy: the single-checkpoint window on Rd, which it never folds */
+    return orc_replay_window(dk, dv, L, Rd, rdt, ek, ev, idt, ealpha, ebeta, meta, T, q, k, v, a, b, A_log,
+                             dt_bias, out);
+}
+
+int orc_replay2_flush(int dk, int dv, int L, void* M, int mdt, void* Rd, int rdt, const void* ek, const void* ev,
+                      int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force) {
+    if (meta[0] < 0 || meta[0] > L || meta[1] - meta[2] != meta[0]) return -2;
+    if (force ? meta[0] > 0 : meta[0] == L) fold2(dk, dv, M, mdt, Rd, rdt, ek, ev, idt, ealpha, ebeta, meta);
+    return 0;
+}
+
 int orc_replay_flush(int dk, int dv, int L, void* S0, int sdt, const void* ek, const void* ev,
                      int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force) {
     if (meta[0] < 0 || meta[0] > L || meta[1] - meta[2] != meta[0]) return -2;

@@ -87,6 +87,18 @@ int orc_replay_flush(int dk, int dv, int L, void* S0, int sdt, const void* ek, c
                      int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force);
 int orc_replay_rollback(int32_t* meta, int T, int accepted);
 
+/* ReplaySSM with a high-precision checkpoint M (mdt) for the recurrence and a
+ * low-precision copy Rd (rdt, dv*dk elements) for reading. Outputs, and every
+ * entry's prediction S^T k, come from the state rebuilt from Rd. A fold
+ * applies each entry's update, taken from that Rd-based rebuild, to M as
+ * well; then it stores M rounded to mdt and Rd as the stored M rounded to
+ * rdt. The window never folds Rd by itself. Codes as orc_replay_window. */
+int orc_replay2_window(int dk, int dv, int L, void* M, int mdt, void* Rd, int rdt, void* ek, void* ev, int idt,
+                       double* ealpha, double* ebeta, int32_t* meta, int T, const void* q, const void* k,
+                       const void* v, const double* a, const double* b, double A_log, double dt_bias, double* out);
+int orc_replay2_flush(int dk, int dv, int L, void* M, int mdt, void* Rd, int rdt, const void* ek, const void* ev,
+                      int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,120 @@
+"""Pins of the oracle's two-checkpoint ReplaySSM mode (oracle.ReplayHead with
+read_dtype): a high-precision checkpoint for the recurrence and a
+low-precision copy for reading. Fixed independently of the mode's code:
+
+- with fp64 for both copies it is the single-checkpoint replay, exactly, through
+  folds, verify windows and rollbacks;
+- between folds its outputs are those of a single-checkpoint replay whose
+  checkpoint is the current read copy;
+- after a fold the read copy is the stored master rounded to the read dtype;
+- dk = dv = 1: the fold's closed form, whose prediction comes from the read copy
+  (a fold that predicted from the master gives a different value);
+- beta = 0: the fold is the pure decay of the master.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+EPS = 1e-6
+
+
+def _tokens(r, T, dk, dv):
+    return (r.standard_normal((T, dk)), r.standard_normal((T, dk)), r.standard_normal((T, dv)),
+            r.standard_normal(T), r.standard_normal(T))
+
+
+def _drive(heads, steps, dk, dv, seed, A_log=0.4, dt_bias=-0.2, windows=True):
+    """Feed the same token stream to every head: steps of one token, and (optionally) T=3 windows
+    with rollbacks. Returns the list of per-call outputs of every head."""
+    r = np.random.default_rng(seed)
+    outs = [[] for _ in heads]
+    for s in range(steps):
+        T = 3 if windows and s % 4 == 3 else 1
+        q, k, v, a, b = _tokens(r, T, dk, dv)
+        for i, hd in enumerate(heads):
+            outs[i].append(hd.window(q, k, v, a, b, A_log, dt_bias))
+        if T > 1:
+            acc = int(r.integers(0, T))
+            for hd in heads:
+                hd.rollback(T, acc)
+    return outs
+
+
+def test_fp64_copies_equal_the_single_checkpoint_replay():
+    dk, dv, L = 8, 6, 5
+    S0 = np.random.default_rng(1).standard_normal((dv, dk))
+    two = oracle.ReplayHead(S0, "f64", "f64", L, read_dtype="f64")
+    one = oracle.ReplayHead(S0, "f64", "f64", L)
+    o2, o1 = _drive([two, one], 30, dk, dv, seed=2)
+    for a, b in zip(o2, o1):
+        assert np.array_equal(a, b)
+    assert np.array_equal(two.S0, one.S0) and np.array_equal(two.Sr, one.S0)
+    two.flush(True), one.flush(True)
+    assert np.array_equal(two.S0, one.S0)
+
+
+@pytest.mark.parametrize("mdt,rdt", [("f32", "bf16"), ("f32", "f16"), ("f64", "bf16")])
+def test_outputs_read_the_copy_and_folds_refresh_it(mdt, rdt):
+    dk, dv, L = 16, 8, 4
+    r = np.random.default_rng(3)
+    S0 = oracle.round_to(0.3 * r.standard_normal((dv, dk)), mdt)
+    two = oracle.ReplayHead(S0, mdt, "f32", L, read_dtype=rdt)
+    assert np.array_equal(two.Sr, oracle.round_to(oracle.load(S0, mdt), rdt))
+    mirror = oracle.ReplayHead(two.Sr, rdt, "f32", L)  # a single-checkpoint replay on the read copy
+    folds = 0
+    for s in range(25):
+        q, k, v, a, b = _tokens(r, 1, dk, dv)
+        a = a.astype(np.float32).astype(np.float64)  # inputs given in fp32
+        if two.count + 1 > L:  # this call folds: the mirror restarts from the refreshed copy afterwards
+            out = two.window(q.astype(np.float32), k.astype(np.float32), v.astype(np.float32), a, b, 0.3, 0.1)
+            folds += 1
+            assert np.array_equal(two.Sr, oracle.round_to(oracle.load(two.S0, mdt), rdt))
+            mirror = oracle.ReplayHead(two.Sr, rdt, "f32", L, pos=two.ckpt_pos)
+            ref = mirror.window(q.astype(np.float32), k.astype(np.float32), v.astype(np.float32), a, b, 0.3, 0.1)
+        else:
+            out = two.window(q.astype(np.float32), k.astype(np.float32), v.astype(np.float32), a, b, 0.3, 0.1)
+            ref = mirror.window(q.astype(np.float32), k.astype(np.float32), v.astype(np.float32), a, b, 0.3, 0.1)
+        assert np.array_equal(out, ref), s
+    assert folds >= 4
+
+
+def test_scalar_fold_predicts_from_the_read_copy():
+    """dk = dv = 1 with one buffered entry: the fold gives m' = alpha m + k w with
+    w = beta (v - alpha r k), r the read copy, k = x / sqrt(x^2 + eps)."""
+    m = 0.7372654321  # not a bf16 value, so the read copy differs from the master
+    two = oracle.ReplayHead(np.array([[m]]), "f64", "f64", 1, read_dtype="bf16")
+    r_ = float(oracle.load(two.Sr, "bf16")[0, 0])
+    assert r_ != m
+    x, v, a_in, b_in = 1.25, -0.6, 0.3, 0.8
+    A_log, dt_bias = 0.2, -0.1
+    alpha, beta = oracle.gating(A_log, dt_bias, a_in, b_in)
+    two.window(np.array([[0.5]]), np.array([[x]]), np.array([[v]]), np.array([a_in]), np.array([b_in]), A_log,
+               dt_bias)
+    # the next window folds that entry first (L = 1)
+    two.window(np.array([[0.5]]), np.array([[x]]), np.array([[v]]), np.array([a_in]), np.array([b_in]), A_log,
+               dt_bias)
+    kn = x / math.sqrt(x * x + EPS)
+    w = beta * (v - alpha * r_ * kn)
+    expect = alpha * m + kn * w
+    assert two.S0[0, 0] == pytest.approx(expect, rel=1e-15)
+    wrong = alpha * m + kn * beta * (v - alpha * m * kn)  # a prediction from the master instead
+    assert abs(two.S0[0, 0] - wrong) > 1e-6
+    assert float(oracle.load(two.Sr, "bf16")[0, 0]) == float(oracle.load(oracle.round_to(np.array([expect]), "bf16"),
+                                                                          "bf16")[0])
+
+
+def test_pure_decay_fold():
+    """b = -inf: beta = 0, so a fold scales the master by the product of the buffered alphas."""
+    dk, dv, L = 8, 4, 3
+    r = np.random.default_rng(5)
+    M0 = r.standard_normal((dv, dk))
+    two = oracle.ReplayHead(M0, "f64", "f64", L, read_dtype="bf16")
+    A_log, dt_bias = 0.0, 0.5
+    for _ in range(L + 1):  # L entries, then the fold
+        q, k, v, _, _ = _tokens(r, 1, dk, dv)
+        two.window(q, k, v, np.array([-dt_bias]), np.array([-np.inf]), A_log, dt_bias)
+    assert np.allclose(two.S0, 0.5 ** L * M0, rtol=1e-14, atol=0)
+    assert np.array_equal(two.Sr, oracle.round_to(two.S0, "bf16"))
