@@ -229,6 +229,20 @@ __device__ __forceinline__ void store_elem(void* base, int64_t idx, int dt, floa
     }
 }
 
+// N (4 or 8) floats stored as N consecutive 16-bit elements (bf16 or fp16,
+// round-to-nearest-even) at dst, which is aligned to 2N bytes.
+template <int N>
+__device__ __forceinline__ void store_run16(char* dst, const float* x, int dt) {
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i)
+        w[i] = dt == GDN_BF16 ? pack_bf16x2(x[2 * i], x[2 * i + 1]) : pack_f16x2(x[2 * i], x[2 * i + 1]);
+    if constexpr (N == 4)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // N consecutive runtime-typed elements from shared memory, starting at
 // element `first` (first * size aligned to N * size, N in {4, 8}).
 template <int N>

@@ -87,6 +87,12 @@ struct ReplayArgs {
     int64_t num_slots;
     int B, Hk, Hv, dv, L, T, force;
     int in_dtype, out_dtype;
+    // Two-checkpoint mode: a fold also writes its rounded rows to ckpt_copy (copy_dtype, 16-bit),
+    // the low-precision copy that the step reads. A launch with T = 0 folds every unit with
+    // count + fold_need > L (or, with force, count > 0); a launch with no_fold refuses a unit
+    // that would have to fold (it runs on the read copy, which never folds by itself).
+    void* ckpt_copy;
+    int copy_dtype, fold_need, no_fold;
     int rows, nchunk;
     int nstage, nhead;  // chunk and head ring depths
     float q_scale;
@@ -259,18 +265,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     if (ck0 < 0 || count < 0 || count > L) {
                         set_error(p.dev_err, GDN_DEVERR_RING);
                     } else if (T > 0) {
-                        slot = s;
                         fold = count + T > L;
+                        if (fold && p.no_fold) {
+                            set_error(p.dev_err, GDN_DEVERR_RING);
+                        } else {
+                            slot = s;
 #pragma unroll
-                        for (int t = 0; t < TMAX; ++t) {
-                            if (t < T) {
-                                const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
-                                gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
-                                      load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
+                            for (int t = 0; t < TMAX; ++t) {
+                                if (t < T) {
+                                    const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
+                                    gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
+                                          load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
+                                }
                             }
                         }
                     } else {
-                        fold = p.force ? count > 0 : count == L;
+                        fold = p.force ? count > 0 : count + p.fold_need > L;
                         slot = fold ? s : -2;
                     }
                 }
@@ -641,6 +651,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                             const uint4 packed = Store<ST>::pack(s[r] + cc * C::VEC);
                             *reinterpret_cast<uint4*>(dst + pos_of(cc) * (int)sizeof(ST)) = packed;
                             Store<ST>::unpack(packed, s[r] + cc * C::VEC);
+                        }
+                        if (p.ckpt_copy) {  // the read copy: the stored row, rounded again to 16 bits
+                            char* cdst = static_cast<char*>(p.ckpt_copy) +
+                                         (((int64_t)slot * p.Hv + h) * p.dv + j[r]) * DK * 2;
+#pragma unroll
+                            for (int cc = 0; cc < C::NC; ++cc)
+                                store_run16<C::VEC>(cdst + pos_of(cc) * 2, s[r] + cc * C::VEC, p.copy_dtype);
                         }
                     }
                 };

@@ -38,7 +38,7 @@ class gdn_dims(C.Structure):
 class gdn_replay_cache(C.Structure):
     _fields_ = [("ckpt", C.c_void_p), ("ckpt_dtype", C.c_int32), ("ring_k", C.c_void_p), ("ring_v", C.c_void_p),
                 ("ring_dtype", C.c_int32), ("ring_rec", C.c_void_p), ("pos", C.c_void_p),
-                ("ckpt_pos", C.c_void_p), ("L", C.c_int32)]
+                ("ckpt_pos", C.c_void_p), ("L", C.c_int32), ("ckpt_read", C.c_void_p), ("read_dtype", C.c_int32)]
 
 
 _lib = None
@@ -149,30 +149,35 @@ class ReplayCache:
 
     ckpt [num_slots, Hv, dv, dk]; ring_k [num_slots, Hv, L, dk];
     ring_v [num_slots, Hv, L, dv]; ring_rec [num_slots, Hv, L, 4 + dv] fp32;
-    pos, ckpt_pos [num_slots, Hv] int32.
+    pos, ckpt_pos [num_slots, Hv] int32; ckpt_read: None, or the low-precision read copy
+    [num_slots, Hv, dv, dk] (bf16/fp16) of an fp32 ckpt.
     """
 
-    def __init__(self, ckpt, ring_k, ring_v, ring_rec, pos, ckpt_pos, L: int):
+    def __init__(self, ckpt, ring_k, ring_v, ring_rec, pos, ckpt_pos, L: int, ckpt_read=None):
         self.ckpt, self.ring_k, self.ring_v, self.ring_rec = ckpt, ring_k, ring_v, ring_rec
         self.pos, self.ckpt_pos, self.L = pos, ckpt_pos, int(L)
+        self.ckpt_read = ckpt_read
 
     @classmethod
     def allocate(cls, num_slots, Hv, dk, dv, L, ckpt_dtype=torch.float32, ring_dtype=torch.bfloat16,
-                 device="cuda") -> "ReplayCache":
-        """Zero-initialised cache; the caller then writes checkpoints and pointers."""
+                 device="cuda", read_dtype=None) -> "ReplayCache":
+        """Zero-initialised cache; the caller then writes checkpoints (and the read copy, the
+        checkpoint rounded, when read_dtype is given) and pointers."""
         z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=device)
+        read = None if read_dtype is None else z((num_slots, Hv, dv, dk), read_dtype)
         return cls(z((num_slots, Hv, dv, dk), ckpt_dtype), z((num_slots, Hv, L, dk), ring_dtype),
                    z((num_slots, Hv, L, dv), ring_dtype), z((num_slots, Hv, L, 4 + dv), torch.float32),
-                   z((num_slots, Hv), torch.int32), z((num_slots, Hv), torch.int32), L)
+                   z((num_slots, Hv), torch.int32), z((num_slots, Hv), torch.int32), L, read)
 
     @property
     def shape(self):
         return self.ckpt.shape  # num_slots, Hv, dv, dk
 
     def c_struct(self) -> gdn_replay_cache:
+        read = self.ckpt_read
         return gdn_replay_cache(_ptr(self.ckpt), _code(self.ckpt), _ptr(self.ring_k), _ptr(self.ring_v),
                                 _code(self.ring_k), _ptr(self.ring_rec), _ptr(self.pos), _ptr(self.ckpt_pos),
-                                self.L)
+                                self.L, None if read is None else _ptr(read), 0 if read is None else _code(read))
 
 
 def _replay_dims(cache: ReplayCache, slots, q) -> gdn_dims:

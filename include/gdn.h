@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 
 /* Host-side return codes. */
 #define GDN_OK 0
@@ -160,6 +160,18 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
  * A fold -- ckpt <- round(S after all buffered entries), ckpt_pos <- pos --
  * happens exactly when appending the call's tokens would overflow the ring
  * (count + T > L), before they are appended, or on gdn_replay_flush.
+ *
+ * ckpt_read  NULL, or a low-precision read copy [num_slots][Hv][dv][dk] of
+ *            read_dtype (bf16 or fp16; ckpt_dtype must then be fp32): the
+ *            high-precision checkpoint for the recurrence and the
+ *            low-precision copy for reading of the AREX ReplaySSM article
+ *            (section "缓存输入而非状态", its precision paragraph). Every
+ *            output and every prediction S^T k then reads ckpt_read; only a
+ *            fold reads ckpt, applies the buffered entries' updates to it,
+ *            stores it, and rewrites ckpt_read as the stored value rounded to
+ *            read_dtype. A fresh sequence: ckpt_read = ckpt rounded. Each call
+ *            then runs a fold pass over the fp32 checkpoint before the step
+ *            itself (two launches on the stream).
  */
 typedef struct gdn_replay_cache {
     void* ckpt;
@@ -171,6 +183,8 @@ typedef struct gdn_replay_cache {
     int32_t* pos;
     int32_t* ckpt_pos;
     int32_t L;
+    void* ckpt_read;
+    int32_t read_dtype;
 } gdn_replay_cache;
 
 /*

@@ -57,16 +57,21 @@ def maxabs(a: np.ndarray, b: np.ndarray) -> float:
 class GpuReplay:
     """A ReplaySSM cache on the GPU built from a workload's initial pool."""
 
-    def __init__(self, w: wl.Workload, pool_host: np.ndarray):
+    def __init__(self, w: wl.Workload, pool_host: np.ndarray, read_dtype=None):
         num_slots = pool_host.shape[0]
         self.cache = gdn.ReplayCache.allocate(num_slots, w.Hv, w.dk, w.dv, w.L, TORCH_DT[w.state_dtype],
-                                              TORCH_DT[w.in_dtype])
+                                              TORCH_DT[w.in_dtype],
+                                              read_dtype=None if read_dtype is None else TORCH_DT[read_dtype])
         self.cache.ckpt.copy_(dev(pool_host, w.state_dtype))
+        if read_dtype is not None:  # a fresh sequence's read copy is its checkpoint rounded
+            self.cache.ckpt_read.copy_(dev(oracle.round_to(oracle.load(pool_host, w.state_dtype), read_dtype),
+                                           read_dtype))
         self.w = w
 
 
-def replay_oracle_heads(w: wl.Workload, pool_host: np.ndarray, slots: np.ndarray, units) -> dict:
-    return {(b, h): oracle.ReplayHead(pool_host[slots[b], h], w.state_dtype, w.in_dtype, w.L) for b, h in units}
+def replay_oracle_heads(w: wl.Workload, pool_host: np.ndarray, slots: np.ndarray, units, read_dtype=None) -> dict:
+    return {(b, h): oracle.ReplayHead(pool_host[slots[b], h], w.state_dtype, w.in_dtype, w.L, read_dtype=read_dtype)
+            for b, h in units}
 
 
 def oracle_window(head: oracle.ReplayHead, x: dict, w: wl.Workload, b: int, h: int, A_log, dt_bias) -> np.ndarray:

@@ -35,22 +35,24 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert gdn.gdn_abi_version() == 1
+    assert gdn.gdn_abi_version() == 2
 
 
 def test_struct_layout_matches_header(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdn.h"\nint main(void){'
-                   'printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(gdn_dims), offsetof(gdn_dims, num_slots),'
+                   'printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(gdn_dims), offsetof(gdn_dims, num_slots),'
                    'sizeof(gdn_replay_cache), offsetof(gdn_replay_cache, ring_rec),'
-                   'offsetof(gdn_replay_cache, ckpt_pos), offsetof(gdn_replay_cache, L)); return 0;}\n')
+                   'offsetof(gdn_replay_cache, ckpt_pos), offsetof(gdn_replay_cache, L),'
+                   'offsetof(gdn_replay_cache, ckpt_read), offsetof(gdn_replay_cache, read_dtype)); return 0;}\n')
     exe = tmp_path / "layout"
     inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
     subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     want = [C.sizeof(gdn.gdn_dims), gdn.gdn_dims.num_slots.offset, C.sizeof(gdn.gdn_replay_cache),
             gdn.gdn_replay_cache.ring_rec.offset, gdn.gdn_replay_cache.ckpt_pos.offset,
-            gdn.gdn_replay_cache.L.offset]
+            gdn.gdn_replay_cache.L.offset, gdn.gdn_replay_cache.ckpt_read.offset,
+            gdn.gdn_replay_cache.read_dtype.offset]
     assert got == want
 
 
@@ -64,8 +66,8 @@ def _decode(lib, dims, pool=FAKE, sdt=0, slots=FAKE, q=FAKE, k=FAKE, v=FAKE, a=F
     return lib.gdn_decode_step(d, pool, sdt, slots, q, k, v, a, b, idt, A, dt, out, odt, err, None)
 
 
-def _cache(L=16, ckpt=FAKE, cdt=0, rdt=1):
-    return gdn.gdn_replay_cache(ckpt, cdt, FAKE, FAKE, rdt, FAKE, FAKE, FAKE, L)
+def _cache(L=16, ckpt=FAKE, cdt=0, rdt=1, read=None, read_dt=0):
+    return gdn.gdn_replay_cache(ckpt, cdt, FAKE, FAKE, rdt, FAKE, FAKE, FAKE, L, read, read_dt)
 
 
 def test_decode_rejections(lib):
@@ -120,6 +122,10 @@ def test_replay_rejections(lib):
     assert _verify(lib, _dims(dv=48), _cache(), 4) == -3  # replay needs dv % 32 == 0
     assert lib.gdn_rollback(C.byref(d), C.byref(_cache(L=4)), FAKE, FAKE, 5, FAKE, None) == -4
     assert lib.gdn_rollback(C.byref(d), C.byref(_cache()), FAKE, None, 4, FAKE, None) == -1
+    # a read copy needs an fp32 checkpoint and a bf16/fp16 copy, 16-byte aligned
+    assert _verify(lib, d, _cache(read=FAKE, read_dt=0), 4) == -2
+    assert _verify(lib, d, _cache(cdt=1, read=FAKE, read_dt=1), 4) == -2
+    assert _verify(lib, d, _cache(read=FAKE + 8, read_dt=1), 4) == -5
 
 
 def test_binding_refuses_host_tensors(lib):

@@ -32,14 +32,15 @@ def _lib():
 
 
 class Harness:
-    def __init__(self, w: wl.Workload, units=None):
+    def __init__(self, w: wl.Workload, units=None, read_dtype=None):
         self.w = w
+        self.rdt = read_dtype
         self.pool = wl.initial_pool(w)
         self.slots = wl.slots(w)
         self.A_log, self.dt_bias = wl.head_params(w)
-        self.g = GpuReplay(w, self.pool)
+        self.g = GpuReplay(w, self.pool, read_dtype)
         self.units = units if units is not None else [(b, h) for b in range(w.B) for h in range(w.Hv)]
-        self.heads = replay_oracle_heads(w, self.pool, self.slots, self.units)
+        self.heads = replay_oracle_heads(w, self.pool, self.slots, self.units, read_dtype)
         self.A_d = torch.from_numpy(self.A_log).cuda()
         self.dt_d = torch.from_numpy(self.dt_bias).cuda()
         self.err = dev_err()
@@ -91,6 +92,12 @@ class Harness:
             S0 = to_f64(c.ckpt[s, h])
             d = maxabs(S0, oracle.load(hd.S0, w.state_dtype))
             assert d <= TOL[w.state_dtype], f"checkpoint of {(b, h)}: {d:.3e}"
+            if self.rdt is not None:
+                # the read copy: the stored checkpoint rounded, bit-exactly, and near the oracle's copy
+                rd = c.ckpt_read[s, h].float().double().cpu().numpy()
+                assert np.array_equal(rd, oracle.load(oracle.round_to(S0, self.rdt), self.rdt)), f"copy of {(b, h)}"
+                d = maxabs(rd, oracle.load(hd.Sr, self.rdt))
+                assert d <= TOL[self.rdt], f"read copy of {(b, h)}: {d:.3e}"
             for e in range(hd.count):
                 i = (hd.ckpt_pos + e) % w.L
                 assert np.array_equal(rk[s, h, i].view(np.uint8), hd.ek[e].view(np.uint8)), f"ring k {(b, h, e)}"
@@ -208,3 +215,31 @@ def test_replay_b256_sampled(name):
 @pytest.mark.parametrize("name", ["verify_b256_f32", "verify_b256_bf16"])
 def test_verify_b256_sampled(name):
     _sampled(name, 8)
+
+
+@pytest.mark.parametrize("rdt", ["bf16", "f16"])
+@pytest.mark.parametrize("T,L", [(1, 4), (3, 8)])
+def test_read_copy_small_all_units(rdt, T, L):
+    # fp32 checkpoint for the recurrence, bf16/fp16 copy for reading; 3 x 4 folds at least
+    w = wl.Workload("rc", B=20, Hk=2, Hv=8, dk=64, dv=64, steps=12, state_dtype="f32", in_dtype="bf16", L=L, T=T,
+                    seed=41)
+    H = Harness(w, read_dtype=rdt)
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, T, f"round {r}")
+        if T > 1:
+            H.rollback(wl.accepted(w, r), T)
+    H.check_state()
+    gdn.gdn_replay_flush(H.g.cache, torch.from_numpy(H.slots).cuda(), True, H.err)
+    for u in H.units:
+        H.heads[u].flush(True)
+    H.check_state()
+
+
+@pytest.mark.slow
+def test_read_copy_b256_sampled():
+    w = wl.WORKLOADS["replay_b256_f32"]
+    H = Harness(w, sample_units(w.B, w.Hv, 8, seed=6), read_dtype="bf16")
+    H.prefill(wl.start_offsets(w))
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, 1, f"round {r}")
+    H.check_state()
