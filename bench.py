@@ -48,17 +48,25 @@ def decode_bytes_per_token(state_bytes: int, in_bytes: int = 2, out_bytes: int =
             HV * DV * out_bytes + 4)
 
 
-def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes: int = 2, out_bytes: int = 4,
+                      read_bytes: int = 0) -> int:
     """Algorithmic bytes of one ReplaySSM call for one (sequence, value head):
     checkpoint read, the `count` buffered ring entries read (raw k + the fp32
     record {alpha, beta, w}), T tokens of inputs (q/k shared by Hv/Hk value
     heads), T appended entries (raw k, raw v, record), T outputs, pointers,
-    and on a fold the checkpoint write."""
+    and on a fold the checkpoint write. With a read copy of `read_bytes` per
+    element, a call that does not fold reads only the copy; a fold reads and
+    writes the master and writes the copy, and the tokens after it use the
+    fresh copy without reading it back (the count of a fused kernel)."""
     rec = (4 + DV) * 4
-    state = DK * DV * ckpt_bytes
+    cells = DK * DV
+    if read_bytes:
+        state = cells * (2 * ckpt_bytes + read_bytes) if fold else cells * read_bytes
+    else:
+        state = cells * ckpt_bytes * (2 if fold else 1)
     inputs = T * (2 * DK * in_bytes * HK // HV + DV * in_bytes + 2 * in_bytes)
     return (state + count * (DK * in_bytes + rec) + inputs + T * (DK * in_bytes + DV * in_bytes + rec) +
-            T * DV * out_bytes + 16 + (state if fold else 0))
+            T * DV * out_bytes + 16)
 
 
 def spec_bytes_per_seq(T: int, state_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
@@ -326,9 +334,13 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
 
     offsets = wl.start_offsets(wl.WORKLOADS["replay_b256_f32"])
     slot_np = wl.slots(w)
-    for ckname, cdt, cs in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
-        cache = gdn.ReplayCache.allocate(NUM_SLOTS, HV, DK, DV, L_RING, cdt, torch.bfloat16, device=dev)
+    for ckname, cdt, cs, rdt, rs in (("fp32", torch.float32, 4, None, 0), ("bf16", torch.bfloat16, 2, None, 0),
+                                     ("fp32_bf16read", torch.float32, 4, torch.bfloat16, 2)):
+        cache = gdn.ReplayCache.allocate(NUM_SLOTS, HV, DK, DV, L_RING, cdt, torch.bfloat16, device=dev,
+                                         read_dtype=rdt)
         cache.ckpt.normal_(0, 0.1, generator=gen)
+        if rdt is not None:
+            cache.ckpt_read.copy_(cache.ckpt.to(rdt))
         counts = np.zeros(NUM_SLOTS, dtype=np.int64)
         counts[slot_np] = offsets
         cache.pos.copy_(torch.from_numpy(np.repeat(counts[:, None], HV, 1).astype(np.int32)))
@@ -344,7 +356,8 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         cc = c.copy()
         for _ in range(rsteps):  # host replay of the ring counts: fold when an append would overflow
             fold = cc + 1 > L_RING
-            total_bytes += HV * sum(replay_unit_bytes(int(x), 1, bool(f), cs) for x, f in zip(cc, fold))
+            total_bytes += HV * sum(replay_unit_bytes(int(x), 1, bool(f), cs, read_bytes=rs)
+                                    for x, f in zip(cc, fold))
             cc = np.where(fold, 0, cc) + 1
         el, lm = timed(rstep, rsteps, 3)
         gbs = total_bytes / rsteps / (lm / 1e3) / 1e9
@@ -352,8 +365,9 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "tokens_per_s": world * B * rsteps / (el / 1e3), "us_per_step": el / rsteps * 1e3, "hbm_gbs": gbs,
             "frac": gbs / peak, "bytes_per_token": total_bytes / rsteps / B, "L": L_RING,
             "start_offsets": "uniform in [0, 15]",
-            "state_write_bytes_per_token": HV * DK * DV * cs / L_RING}
-        result["gpu_launches"] += rsteps
+            "state_write_bytes_per_token": HV * DK * DV * (cs + rs) / L_RING,
+            "launches_per_step": 2 if rdt is not None else 1}
+        result["gpu_launches"] += rsteps * (2 if rdt is not None else 1)
 
         # verify T=4 + rollback, accepted uniform in {0..3}
         T = T_VERIFY
@@ -374,7 +388,8 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         vbytes = 0
         for _ in range(3 + vrounds):  # host replay of the counts through warm-up and timed rounds
             fold = cv + T > L_RING
-            vbytes_round = HV * sum(replay_unit_bytes(int(x), T, bool(f), cs) for x, f in zip(cv, fold))
+            vbytes_round = HV * sum(replay_unit_bytes(int(x), T, bool(f), cs, read_bytes=rs)
+                                   for x, f in zip(cv, fold))
             cv = np.where(fold, 0, cv) + 1 + acc_np
             vbytes = vbytes_round  # bytes of the last round (the counts cycle; rounds differ little)
         accepted_tokens = float((acc.float() + 1).sum().item())
@@ -384,7 +399,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "accepted_tokens_per_s": world * accepted_tokens * vrounds / (el / 1e3),
             "us_per_round": el / vrounds * 1e3, "T": T, "L": L_RING, "hbm_gbs": vgbs, "frac": vgbs / peak,
             "bytes_per_round": vbytes}
-        result["gpu_launches"] += 2 * vrounds
+        result["gpu_launches"] += (3 if rdt is not None else 2) * vrounds
         del cache
     # the baseline the verify window replaces: T=4 window with one state copy per token
     T = T_VERIFY
@@ -473,7 +488,8 @@ def run_case(args) -> None:
     """Run a few untimed launches of one kernel for a profiler (no JSON line).
 
     decode:  B sequences, fp32/bf16/fp16 state pool of 2B slots.
-    replay:  ReplaySSM steps, L=16 ring pre-filled to start offsets in [0, 15].
+    replay:  ReplaySSM steps, L=16 ring pre-filled to start offsets in [0, 15]; with
+             --read-dtype, an fp32 checkpoint plus a read copy of that dtype.
     verify:  T=4 verify windows + rollbacks on the same cache.
     spec:    T=4 speculative steps with one state copy per window token, pool of 5B slots.
     """
@@ -510,8 +526,11 @@ def run_case(args) -> None:
             gdn.gdn_spec_step(pool, src, dst, q, k, v, a, b, A_log, dt_bias, out, err)
     else:
         T = T_VERIFY if args.case == "verify" else 1
-        cache = gdn.ReplayCache.allocate(2 * Bc, HV, DK, DV, L_RING, sdt, torch.bfloat16, device=dev)
+        rdt = {None: None, "bf16": torch.bfloat16, "f16": torch.float16}[args.read_dtype]
+        cache = gdn.ReplayCache.allocate(2 * Bc, HV, DK, DV, L_RING, sdt, torch.bfloat16, device=dev, read_dtype=rdt)
         cache.ckpt.normal_(0, 0.1, generator=g)
+        if rdt is not None:
+            cache.ckpt_read.copy_(cache.ckpt.to(rdt))
         off = torch.randint(0, L_RING, (2 * Bc, 1), generator=g, device=dev).to(torch.int32)
         cache.pos.copy_(off.expand(2 * Bc, HV))
         q, k, v, a, b = rnd(Bc, T, HK, DK), rnd(Bc, T, HK, DK), rnd(Bc, T, HV, DV), rnd(Bc, T, HV), rnd(Bc, T, HV)
@@ -543,6 +562,8 @@ def main():
                     help="run --steps untimed launches of one kernel for a profiler and exit")
     ap.add_argument("--B", type=int, default=B, help="batch of --case")
     ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16", "f16"], help="state dtype of --case")
+    ap.add_argument("--read-dtype", default=None, choices=["bf16", "f16"],
+                    help="read copy of the replay/verify checkpoint of --case (needs --state-dtype f32)")
     args = ap.parse_args()
     if args.case:
         run_case(args)
