@@ -57,7 +57,7 @@ def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes:
     and on a fold the checkpoint write. With a read copy of `read_bytes` per
     element, a call that does not fold reads only the copy; a fold reads and
     writes the master and writes the copy, and the tokens after it use the
-    fresh copy without reading it back (the count of a fused kernel)."""
+    fresh copy without reading it back."""
     rec = (4 + DV) * 4
     cells = DK * DV
     if read_bytes:
@@ -365,9 +365,8 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "tokens_per_s": world * B * rsteps / (el / 1e3), "us_per_step": el / rsteps * 1e3, "hbm_gbs": gbs,
             "frac": gbs / peak, "bytes_per_token": total_bytes / rsteps / B, "L": L_RING,
             "start_offsets": "uniform in [0, 15]",
-            "state_write_bytes_per_token": HV * DK * DV * (cs + rs) / L_RING,
-            "launches_per_step": 2 if rdt is not None else 1}
-        result["gpu_launches"] += rsteps * (2 if rdt is not None else 1)
+            "state_write_bytes_per_token": HV * DK * DV * (cs + rs) / L_RING}
+        result["gpu_launches"] += rsteps
 
         # verify T=4 + rollback, accepted uniform in {0..3}
         T = T_VERIFY
@@ -399,7 +398,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "accepted_tokens_per_s": world * accepted_tokens * vrounds / (el / 1e3),
             "us_per_round": el / vrounds * 1e3, "T": T, "L": L_RING, "hbm_gbs": vgbs, "frac": vgbs / peak,
             "bytes_per_round": vbytes}
-        result["gpu_launches"] += (3 if rdt is not None else 2) * vrounds
+        result["gpu_launches"] += 2 * vrounds
         del cache
     # the baseline the verify window replaces: T=4 window with one state copy per token
     T = T_VERIFY

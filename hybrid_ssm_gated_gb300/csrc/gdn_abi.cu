@@ -122,35 +122,31 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
     p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.L = c->L, p.T = T, p.force = force != 0;
     p.in_dtype = c->ring_dtype, p.out_dtype = T > 0 ? out_dtype : GDN_F32;
     p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
-    p.fold_need = 1;  // a flush without force folds full rings only
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    auto run = [&](gdn::ReplayArgs& a, int ckpt_dtype) -> int {
-        chunking(dims->dk, dims->dv, gdn::dtype_size(ckpt_dtype), a.rows, a.nchunk);
-        const int tmax = a.T <= 1 ? 1 : (a.T <= 4 ? 4 : 8);
-        bool too_big = false;
-        cudaError_t e;
-        if (ckpt_dtype == GDN_F32)
-            e = gdn::dispatch_replay_f32(dims->dk, tmax, a, s, too_big);
-        else if (ckpt_dtype == GDN_BF16)
-            e = gdn::dispatch_replay_bf16(dims->dk, tmax, a, s, too_big);
+    const int tmax = T <= 1 ? 1 : (T <= 4 ? 4 : 8);
+    bool too_big = false;
+    cudaError_t e;
+    if (c->ckpt_read) {
+        // Two checkpoints, one launch: steps read the copy; folds stream the fp32 master, update it
+        // and rewrite the copy. A master chunk holds a whole number of the copy's chunks' items.
+        p.ckpt_copy = c->ckpt_read;
+        chunking(dims->dk, dims->dv, gdn::dtype_size(c->read_dtype), p.rows, p.nchunk);
+        chunking(dims->dk, p.rows, 4, p.mrows, p.mnchunk);
+        p.mnchunk = dims->dv / p.mrows;
+        e = c->read_dtype == GDN_BF16 ? gdn::dispatch_replay_f32_bf16(dims->dk, tmax, p, s, too_big)
+                                      : gdn::dispatch_replay_f32_f16(dims->dk, tmax, p, s, too_big);
+    } else {
+        chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
+        p.mrows = p.rows, p.mnchunk = p.nchunk;
+        if (c->ckpt_dtype == GDN_F32)
+            e = gdn::dispatch_replay_f32(dims->dk, tmax, p, s, too_big);
+        else if (c->ckpt_dtype == GDN_BF16)
+            e = gdn::dispatch_replay_bf16(dims->dk, tmax, p, s, too_big);
         else
-            e = gdn::dispatch_replay_f16(dims->dk, tmax, a, s, too_big);
-        if (too_big)
-            return fail(GDN_ERR_SHAPE, "%s: L=%d, T=%d, dv=%d do not fit in shared memory", fn, c->L, a.T, dims->dv);
-        return launched(e, fn);
-    };
-    if (!c->ckpt_read) return run(p, c->ckpt_dtype);
-    // Two checkpoints: a fold pass over the fp32 checkpoint (it also rewrites the read copy), for
-    // every unit whose ring would overflow this call; then the step itself on the read copy, which
-    // then never needs to fold.
-    gdn::ReplayArgs pf = p;
-    pf.T = 0, pf.force = T > 0 ? 0 : p.force, pf.fold_need = T > 0 ? T : 1, pf.out_dtype = GDN_F32;
-    pf.ckpt_copy = c->ckpt_read, pf.copy_dtype = c->read_dtype;
-    int rc2 = run(pf, GDN_F32);
-    if (rc2 != GDN_OK || T == 0) return rc2;
-    gdn::ReplayArgs pr = p;
-    pr.ckpt = c->ckpt_read, pr.no_fold = 1;
-    return run(pr, c->read_dtype);
+            e = gdn::dispatch_replay_f16(dims->dk, tmax, p, s, too_big);
+    }
+    if (too_big) return fail(GDN_ERR_SHAPE, "%s: L=%d, T=%d, dv=%d do not fit in shared memory", fn, c->L, T, dims->dv);
+    return launched(e, fn);
 }
 
 }  // namespace

@@ -229,18 +229,25 @@ __device__ __forceinline__ void store_elem(void* base, int64_t idx, int dt, floa
     }
 }
 
-// N (4 or 8) floats stored as N consecutive 16-bit elements (bf16 or fp16,
-// round-to-nearest-even) at dst, which is aligned to 2N bytes.
-template <int N>
-__device__ __forceinline__ void store_run16(char* dst, const float* x, int dt) {
-    uint32_t w[N / 2];
+// N consecutive elements of type T at element `first` of a 16-byte aligned
+// row (first * sizeof(T) a multiple of 16, N a multiple of Store<T>::VEC).
+template <typename T, int N>
+__device__ __forceinline__ void load_row_run(const unsigned char* row, int first, float* x) {
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i)
-        w[i] = dt == GDN_BF16 ? pack_bf16x2(x[2 * i], x[2 * i + 1]) : pack_f16x2(x[2 * i], x[2 * i + 1]);
-    if constexpr (N == 4)
-        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int e = 0; e < N; e += Store<T>::VEC)
+        Store<T>::unpack(*reinterpret_cast<const uint4*>(row + (first + e) * (int)sizeof(T)), x + e);
+}
+
+// Store x rounded to T at element `first` of a row (as load_row_run), and
+// replace x by the stored values.
+template <typename T, int N>
+__device__ __forceinline__ void store_row_run(unsigned char* row, int first, float* x) {
+#pragma unroll
+    for (int e = 0; e < N; e += Store<T>::VEC) {
+        const uint4 packed = Store<T>::pack(x + e);
+        *reinterpret_cast<uint4*>(row + (first + e) * (int)sizeof(T)) = packed;
+        Store<T>::unpack(packed, x + e);
+    }
 }
 
 // N consecutive runtime-typed elements from shared memory, starting at

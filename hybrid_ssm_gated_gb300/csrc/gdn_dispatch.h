@@ -18,6 +18,9 @@ cudaError_t dispatch_decode(int state_dtype, int dk, const DecodeArgs& a, cudaSt
 cudaError_t dispatch_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_replay_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+// An fp32 master checkpoint with a bf16 / fp16 read copy.
+cudaError_t dispatch_replay_f32_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_replay_f32_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 
 // tmax in {4, 8}. too_big is set when the layout does not fit in shared memory.
 cudaError_t dispatch_spec_f32(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);

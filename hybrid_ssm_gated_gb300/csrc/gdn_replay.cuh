@@ -48,6 +48,12 @@
 //    Larger windows take one pass per item and scatter the 2T sums of a row
 //    over its lanes; the window's own recursion then passes each w_t across
 //    lanes.
+// Two checkpoints (same article, its paragraph on precision): with a wider
+// master type MT, every unit that does not fold streams the read copy (ST)
+// and one that folds streams the master, folds it in FP32, stores it, and
+// rewrites the copy from the stored rows; the call's tokens then continue
+// from the copy's values, as if it had been read back. A master chunk holds
+// fewer rows, so its items release the chunk with a larger weight.
 // Hand-offs. Every warp visits every head stage in order, so the head and
 // table barriers' parity waits cannot alias. The head barrier takes two
 // arrivals: one arms its copies, the other comes with the metadata once every
@@ -58,6 +64,8 @@
 // warp's release first. Every wait is bounded (GDN_DEVERR_TIMEOUT, then
 // return).
 #pragma once
+
+#include <type_traits>
 
 #include "gdn_decode.cuh"
 #include "gdn_device.cuh"
@@ -87,13 +95,12 @@ struct ReplayArgs {
     int64_t num_slots;
     int B, Hk, Hv, dv, L, T, force;
     int in_dtype, out_dtype;
-    // Two-checkpoint mode: a fold also writes its rounded rows to ckpt_copy (copy_dtype, 16-bit),
-    // the low-precision copy that the step reads. A launch with T = 0 folds every unit with
-    // count + fold_need > L (or, with force, count > 0); a launch with no_fold refuses a unit
-    // that would have to fold (it runs on the read copy, which never folds by itself).
+    // Two-checkpoint mode (master type MT wider than the read type ST): ckpt is the master, which
+    // only folds read and write; ckpt_copy is the read copy, which every other unit reads and
+    // every fold rewrites from the stored master rows.
     void* ckpt_copy;
-    int copy_dtype, fold_need, no_fold;
-    int rows, nchunk;
+    int rows, nchunk;    // S0 rows per 16 KB chunk and chunks per unit, read type
+    int mrows, mnchunk;  // the same for the master (equal to rows, nchunk with one checkpoint)
     int nstage, nhead;  // chunk and head ring depths
     float q_scale;
     // shared-memory layout, bytes
@@ -201,9 +208,13 @@ __device__ __forceinline__ void reduce_scatter_values(float (&x)[V], int g) {
     ScatterStep<V, G / 2>::run(x, g);
 }
 
-template <typename ST, int DK, int TMAX, int NCW>
+// ST: the checkpoint that steps and windows read (the read copy in the two-checkpoint mode);
+// MT: the checkpoint that folds read and write (ST itself with one checkpoint).
+template <typename ST, int DK, int TMAX, int NCW, typename MT = ST>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayArgs p) {
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
+    constexpr bool MIXED = !std::is_same<ST, MT>::value;
+    constexpr int MROW_BYTES = DK * (int)sizeof(MT);  // a master row
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* chunks = smem;
     unsigned char* heads = smem + p.heads_off;
@@ -218,6 +229,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ipu = p.dv / C::ITEM;    // items per unit
     const int ipc = p.rows / C::ITEM;  // items per chunk
+    // a fold unit's master chunks hold fewer rows than the read copy's: their sub-items release
+    // with weight fw, so that every chunk fill takes ipc * SUB releases
+    const int fw = MIXED ? ipc / (p.mrows / C::ITEM) : 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&cfull[s], 1), mbar_init(&cempty[s], ipc * C::SUB);
         for (int s = 0; s < NH; ++s)
@@ -266,21 +280,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         set_error(p.dev_err, GDN_DEVERR_RING);
                     } else if (T > 0) {
                         fold = count + T > L;
-                        if (fold && p.no_fold) {
-                            set_error(p.dev_err, GDN_DEVERR_RING);
-                        } else {
-                            slot = s;
+                        slot = s;
 #pragma unroll
-                            for (int t = 0; t < TMAX; ++t) {
-                                if (t < T) {
-                                    const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
-                                    gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
-                                          load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
-                                }
+                        for (int t = 0; t < TMAX; ++t) {
+                            if (t < T) {
+                                const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
+                                gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
+                                      load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
                             }
                         }
                     } else {
-                        fold = p.force ? count > 0 : count + p.fold_need > L;
+                        fold = p.force ? count > 0 : count + 1 > L;
                         slot = fold ? s : -2;
                     }
                 }
@@ -331,13 +341,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 }
                 const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
                 const int64_t unit_ring = ((int64_t)s_i * p.Hv + h) * L;
+                // a fold unit streams the master checkpoint, any other the one steps read
+                const bool fm = MIXED && f_i;
+                const int nck = fm ? p.mnchunk : p.nchunk;
+                const uint32_t ub = fm ? p.mrows * MROW_BYTES : cbytes;
+                const char* s0 = static_cast<const char*>(MIXED && !f_i ? p.ckpt_copy : p.ckpt) +
+                                 ((int64_t)s_i * p.Hv + h) * p.dv * (fm ? MROW_BYTES : C::ROW_BYTES);
                 // Every copy of the unit is issued by one convergent bulk-copy instruction (one copy
                 // per lane; more rounds only when the chunks do not fit): lanes 0..3T-1 the window's
                 // q/k/v rows, the next four up to two ring ranges (keys, records), then the S0 chunks,
                 // at most NS of them per round so that no lane waits for a stage another lane is
                 // about to fill.
                 const int hj = 3 * T + 4;
-                for (int c0 = 0, round = 0; ok && (round == 0 || c0 < p.nchunk); ++round) {
+                for (int c0 = 0, round = 0; ok && (round == 0 || c0 < nck); ++round) {
                     const int cl0 = round == 0 ? hj : 0;  // first chunk lane of this round
                     const int per = min(NS, 32 - cl0);   // chunk lanes of this round
                     const char* src = nullptr;
@@ -372,18 +388,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         }
                     }
                     const int c = c0 + lane - cl0;
-                    if (lane >= cl0 && lane - cl0 < per && c < p.nchunk) {
+                    if (lane >= cl0 && lane - cl0 < per && c < nck) {
                         const uint32_t mc = m + c;
                         int cs = ms + c;  // stage and fill parity of chunk mc (c < 32, NS >= 2)
                         uint32_t cph = mph;
                         while (cs >= NS) cs -= NS, cph ^= 1;
                         ok = mc < (uint32_t)NS || mbar_wait(&cempty[cs], cph ^ 1);
                         if (ok) {
-                            mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                            src = static_cast<const char*>(p.ckpt) + ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES +
-                                  (int64_t)c * cbytes;
+                            mbar_arrive_expect_tx(&cfull[cs], ub);
+                            src = s0 + (int64_t)c * ub;
                             dst = chunks + cs * CHUNK_BYTES;
-                            bytes = cbytes;
+                            bytes = ub;
                             bar = &cfull[cs];
                             pol = pol_once;
                         }
@@ -392,8 +407,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     if (ok && bytes) bulk_load_hint(dst, src, bytes, bar, pol);
                     c0 += per;
                 }
-                m += p.nchunk;
-                for (ms += p.nchunk; ms >= NS;) ms -= NS, mph ^= 1;
+                m += nck;
+                for (ms += nck; ms >= NS;) ms -= NS, mph ^= 1;
                 publish();
                 if (!ok) break;
             }
@@ -444,6 +459,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
             continue;
         }
         const int count = meta->count, fold = meta->fold, pos0 = meta->pos0;
+        const int upc = MIXED && fold ? p.mrows / C::ITEM : ipc;  // items per chunk of this unit
         const int cpr = fold ? 0 : count;         // ring entries in front of the window
         const int J = T > 1 ? cpr + T : cpr;      // coefficient-table entries: ring, then window (T > 1)
         const int nitems = fold ? ipu * C::SUB : ipu;
@@ -605,7 +621,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // fold: scale of entry f's rank-one term, R(f) / |k_f| (lane f)
                 const float fsc = lane < count ? R * rec[lane * rec_floats + 2] : 0.f;
                 const float gfold = gring;
-                char* gck = static_cast<char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * C::ROW_BYTES;
+                unsigned char* gck =
+                    static_cast<unsigned char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * MROW_BYTES;
                 bool have_coef = false;
 
                 // S0 <- round(G S0 + sum_f A(f) k_f w_f^T) for NR rows s[r] (state rows j[r]) of this
@@ -645,28 +662,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     }
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {
-                        char* dst = gck + (int64_t)j[r] * C::ROW_BYTES;
+                        unsigned char* dst = gck + (int64_t)j[r] * MROW_BYTES;
 #pragma unroll
-                        for (int cc = 0; cc < C::NC; ++cc) {
-                            const uint4 packed = Store<ST>::pack(s[r] + cc * C::VEC);
-                            *reinterpret_cast<uint4*>(dst + pos_of(cc) * (int)sizeof(ST)) = packed;
-                            Store<ST>::unpack(packed, s[r] + cc * C::VEC);
-                        }
-                        if (p.ckpt_copy) {  // the read copy: the stored row, rounded again to 16 bits
-                            char* cdst = static_cast<char*>(p.ckpt_copy) +
-                                         (((int64_t)slot * p.Hv + h) * p.dv + j[r]) * DK * 2;
+                        for (int cc = 0; cc < C::NC; ++cc) store_row_run<MT, C::VEC>(dst, pos_of(cc), s[r] + cc * C::VEC);
+                        if constexpr (MIXED) {  // the read copy: the stored master row, rounded to ST
+                            unsigned char* cdst = static_cast<unsigned char*>(p.ckpt_copy) +
+                                                  (((int64_t)slot * p.Hv + h) * p.dv + j[r]) * C::ROW_BYTES;
 #pragma unroll
                             for (int cc = 0; cc < C::NC; ++cc)
-                                store_run16<C::VEC>(cdst + pos_of(cc) * 2, s[r] + cc * C::VEC, p.copy_dtype);
+                                store_row_run<ST, C::VEC>(cdst, pos_of(cc), s[r] + cc * C::VEC);
                         }
                     }
                 };
+                // row r of a chunk (a master chunk on a fold unit)
                 auto load_state = [&](const unsigned char* tile, int r, float* s) {
+                    if (MIXED && fold) {
 #pragma unroll
-                    for (int cc = 0; cc < C::NC; ++cc)
-                        Store<ST>::unpack(
-                            *reinterpret_cast<const uint4*>(tile + r * C::ROW_BYTES + pos_of(cc) * (int)sizeof(ST)),
-                            s + cc * C::VEC);
+                        for (int cc = 0; cc < C::NC; ++cc)
+                            load_row_run<MT, C::VEC>(tile + r * MROW_BYTES, pos_of(cc), s + cc * C::VEC);
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < C::NC; ++cc)
+                            load_row_run<ST, C::VEC>(tile + r * C::ROW_BYTES, pos_of(cc), s + cc * C::VEC);
+                    }
                 };
 
                 // k.q, the window token's own term in its output (one token)
@@ -679,7 +697,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 }
                 for (int it = i0; it < nitems; it += NCW) {
                     const int bi = fold ? it / C::SUB : it;  // the item (of a fold sub-item)
-                    const int c = bi / ipc;
+                    const int c = bi / upc;
                     int cs = ms + c;  // stage and fill parity of the item's chunk
                     uint32_t cph = mph;
                     while (cs >= NS) cs -= NS, cph ^= 1;
@@ -687,7 +705,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     // stage can be taken for this one
                     if (!(ok = mbar_wait(&cfull[cs], cph))) break;
                     const unsigned char* tile = chunks + cs * CHUNK_BYTES;
-                    const int r0 = (bi - c * ipc) * C::ITEM;  // item's first row within the chunk
+                    const int r0 = (bi - c * upc) * C::ITEM;  // item's first row within the chunk
                     const int j0 = bi * C::ITEM;              // item's first row within the state
 
                     if constexpr (TMAX == 1) {
@@ -704,7 +722,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 jr[r] = j0 + (ps0 + r) * C::RPP + rsub;
                             }
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&cempty[cs]);
+                            if (lane == 0) mbar_arrive_n(&cempty[cs], fw);
                             fold_rows(s, jr);
                             if (T > 0) {
                                 const float al = meta->alpha[0], be = meta->beta[0];
@@ -840,7 +858,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         }
                         if (!ok) break;
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_n(&cempty[cs], fold ? 1 : C::SUB);
+                        if (lane == 0) mbar_arrive_n(&cempty[cs], fold ? fw : C::SUB);
                         if (!have_coef && !(ok = mbar_wait(&cready[hs], hph))) break;  // the window's coefficients
                         have_coef = true;
                         if (lane < np * C::RPP) {
@@ -889,7 +907,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
         __syncwarp();
         if (lane == 0) mbar_arrive(&hempty[hs]);
         base = (base + nitems) % NCW;
-        for (ms += p.nchunk; ms >= NS;) ms -= NS, mph ^= 1;
+        for (ms += MIXED && fold ? p.mnchunk : p.nchunk; ms >= NS;) ms -= NS, mph ^= 1;
     }
     if (!ok && lane == 0) set_error(p.dev_err, GDN_DEVERR_TIMEOUT);
 }

@@ -169,9 +169,11 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
  *            output and every prediction S^T k then reads ckpt_read; only a
  *            fold reads ckpt, applies the buffered entries' updates to it,
  *            stores it, and rewrites ckpt_read as the stored value rounded to
- *            read_dtype. A fresh sequence: ckpt_read = ckpt rounded. Each call
- *            then runs a fold pass over the fp32 checkpoint before the step
- *            itself (two launches on the stream).
+ *            read_dtype. A fresh sequence: ckpt_read = ckpt rounded. One
+ *            launch per call: units that fold stream the fp32 checkpoint,
+ *            the others the read copy; the tokens of a call that folds run
+ *            from the rewritten copy. Both arrays are 16-byte aligned and do
+ *            not overlap.
  */
 typedef struct gdn_replay_cache {
     void* ckpt;
