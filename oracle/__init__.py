@@ -1,8 +1,10 @@
-"""CPU oracle for the GDN decode step and its ReplaySSM mode (ctypes wrapper).
+"""CPU oracle for the GDN and Mamba2 decode steps and their ReplaySSM mode
+(ctypes wrapper).
 
 TEST INFRASTRUCTURE ONLY. Only tests/, the package smoke check and the
 benchmark's CPU-baseline leg may import this package. It shares no code with
-the CUDA library: the arithmetic lives in gdn_oracle.c (plain C, fp64).
+the CUDA library: the arithmetic lives in gdn_oracle.c and mamba2_oracle.c
+(plain C, fp64).
 
 Storage arrays follow hybrid_ssm_gated_gb300.workload: fp32 as float32, fp16 as
 float16, bf16 as uint16 bit patterns, and the oracle-only fp64 as float64.
@@ -43,6 +45,11 @@ def lib() -> C.CDLL:
             "orc_replay_rollback": (I, [P, I, I]),
             "orc_replay2_window": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
             "orc_replay2_flush": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I]),
+            "orc_m2_gating": (None, [D, D, D, P, P]),
+            "orc_m2_decode_head": (None, [I, I, P, I, P, P, P, I, D, D, D, P]),
+            "orc_m2_decode_step": (I, [I, I, I, I, I, I64, P, I, P, P, P, P, P, I, P, P, P, P, I]),
+            "orc_m2_replay_window": (I, [I, I, I, P, I, P, P, I, P, P, P, I, P, P, P, P, D, D, D, P]),
+            "orc_m2_replay_flush": (I, [I, I, I, P, I, P, P, I, P, P, P, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(_lib, name)
@@ -247,6 +254,99 @@ class ReplayHead:
                                          _ptr(self.meta), int(bool(force)))
         if rc != 0:
             raise ValueError(f"oracle replay flush rejected its state (code {rc})")
+
+    def rollback(self, T: int, accepted: int) -> None:
+        rc = lib().orc_replay_rollback(_ptr(self.meta), int(T), int(accepted))
+        if rc != 0:
+            raise ValueError(f"oracle rollback rejected its input (code {rc})")
+
+
+# ---------------------------------------------------------------- Mamba2
+
+
+def m2_gating(A_log: float, dt_bias: float, dt: float) -> tuple[float, float]:
+    """(alpha, delta) of one Mamba2 head: delta = softplus(dt + dt_bias), alpha = exp(-exp(A_log) delta)."""
+    al, de = C.c_double(), C.c_double()
+    lib().orc_m2_gating(float(A_log), float(dt_bias), float(dt), C.addressof(al), C.addressof(de))
+    return al.value, de.value
+
+
+def m2_decode_head(S: np.ndarray, sdt, x, Bv, Cv, idt, alpha: float, delta: float, D: float) -> np.ndarray:
+    """One Mamba2 decode step of one head; S ([P, N] storage array) is updated in place."""
+    assert S.dtype == NPTYPE[_code(sdt)] and S.flags["C_CONTIGUOUS"]
+    P, N = S.shape
+    x, Bv, Cv = _arr(x, idt), _arr(Bv, idt), _arr(Cv, idt)
+    out = np.empty(P, dtype=np.float64)
+    lib().orc_m2_decode_head(N, P, _ptr(S), _code(sdt), _ptr(x), _ptr(Bv), _ptr(Cv), _code(idt), float(alpha),
+                             float(delta), float(D), _ptr(out))
+    return out
+
+
+def m2_decode_step(pool: np.ndarray, sdt, slots, x, dt, Bm, Cm, idt, A_log, dt_bias, D,
+                   nthreads: int = 1) -> tuple[np.ndarray, int]:
+    """One Mamba2 decode step of a batch; pool [num_slots, H, P, N] is updated in place; x [B, H, P],
+    dt [B, H], Bm and Cm [B, G, N]. Returns (out [B, H, P] fp64, number of refused units)."""
+    assert pool.dtype == NPTYPE[_code(sdt)] and pool.flags["C_CONTIGUOUS"]
+    num_slots, H, P, N = pool.shape
+    x, dt, Bm, Cm = (_arr(a, idt) for a in (x, dt, Bm, Cm))
+    B = int(np.asarray(slots).shape[0])
+    G = Bm.size // (B * N)
+    slots = np.ascontiguousarray(slots, dtype=np.int32)
+    A_log, dt_bias, D = (np.ascontiguousarray(a, dtype=np.float32) for a in (A_log, dt_bias, D))
+    out = np.empty((B, H, P), dtype=np.float64)
+    bad = lib().orc_m2_decode_step(B, G, H, N, P, num_slots, _ptr(pool), _code(sdt), _ptr(slots), _ptr(x),
+                                   _ptr(dt), _ptr(Bm), _ptr(Cm), _code(idt), _ptr(A_log), _ptr(dt_bias), _ptr(D),
+                                   _ptr(out), int(nthreads))
+    return out, bad
+
+
+class Mamba2ReplayHead:
+    """ReplaySSM state of one Mamba2 (sequence, head): checkpoint S0 ([P, N] storage array), the
+    buffered entries in arrival order (raw B [L, N] and x [L, P] in the input dtype, alpha and
+    delta [L] fp64) and meta = [count, pos, ckpt_pos]. Rollback is the pointer move of
+    ReplayHead.rollback."""
+
+    def __init__(self, S0: np.ndarray, sdt, idt, L: int, pos: int = 0):
+        self.sdt, self.idt, self.L = _code(sdt), _code(idt), int(L)
+        self.S0 = np.ascontiguousarray(S0, dtype=NPTYPE[self.sdt]).copy()
+        self.P, self.N = self.S0.shape
+        self.eB = np.zeros((L, self.N), dtype=NPTYPE[self.idt])
+        self.ex = np.zeros((L, self.P), dtype=NPTYPE[self.idt])
+        self.ea = np.zeros(L, dtype=np.float64)
+        self.ed = np.zeros(L, dtype=np.float64)
+        self.meta = np.array([0, pos, pos], dtype=np.int32)
+
+    @property
+    def count(self) -> int:
+        return int(self.meta[0])
+
+    @property
+    def pos(self) -> int:
+        return int(self.meta[1])
+
+    @property
+    def ckpt_pos(self) -> int:
+        return int(self.meta[2])
+
+    def window(self, Cw, Bw, xw, dt, A_log: float, dt_bias: float, D: float) -> np.ndarray:
+        """Process T tokens (Cw, Bw [T, N], xw [T, P], dt [T]); returns out [T, P] fp64."""
+        Cw, Bw, xw = _arr(Cw, self.idt), _arr(Bw, self.idt), _arr(xw, self.idt)
+        T = Cw.shape[0]
+        dt = np.ascontiguousarray(dt, dtype=np.float64).reshape(T)
+        out = np.empty((T, self.P), dtype=np.float64)
+        rc = lib().orc_m2_replay_window(self.N, self.P, self.L, _ptr(self.S0), self.sdt, _ptr(self.eB),
+                                        _ptr(self.ex), self.idt, _ptr(self.ea), _ptr(self.ed), _ptr(self.meta), T,
+                                        _ptr(Cw), _ptr(Bw), _ptr(xw), _ptr(dt), float(A_log), float(dt_bias),
+                                        float(D), _ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle Mamba2 replay window rejected its input (code {rc})")
+        return out
+
+    def flush(self, force: bool = True) -> None:
+        rc = lib().orc_m2_replay_flush(self.N, self.P, self.L, _ptr(self.S0), self.sdt, _ptr(self.eB), _ptr(self.ex),
+                                       self.idt, _ptr(self.ea), _ptr(self.ed), _ptr(self.meta), int(bool(force)))
+        if rc != 0:
+            raise ValueError(f"oracle Mamba2 replay flush rejected its state (code {rc})")
 
     def rollback(self, T: int, accepted: int) -> None:
         rc = lib().orc_replay_rollback(_ptr(self.meta), int(T), int(accepted))
