@@ -78,10 +78,12 @@ int check_activations(const char* fn, const void* q, const void* k, const void* 
     return GDN_OK;
 }
 
-int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* c, const int32_t* slots, int32_t T,
-                  int32_t force, const void* q, const void* k, const void* v, const void* a, const void* b,
-                  int32_t in_dtype, const float* A_log, const float* dt_bias, void* out, int32_t out_dtype,
-                  int32_t* dev_err, void* stream) {
+// The replay entry points of both recurrences. Mamba2 passes (C, B, x, dt) as (q, k, v, a), no b, and
+// its skip weights D.
+int replay_common(const char* fn, int rule, const gdn_dims* dims, const gdn_replay_cache* c, const int32_t* slots,
+                  int32_t T, int32_t force, const void* q, const void* k, const void* v, const void* a, const void* b,
+                  int32_t in_dtype, const float* A_log, const float* dt_bias, const float* D, void* out,
+                  int32_t out_dtype, int32_t* dev_err, void* stream) {
     int rc = check_dims(dims, fn);
     if (rc) return rc;
     if (!c) return fail(GDN_ERR_NULL, "%s: cache is NULL", fn);
@@ -95,8 +97,11 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
     if (T > 0) {
         if (T > c->L || T > gdn::WINDOW_MAX)
             return fail(GDN_ERR_WINDOW, "%s: window T=%d exceeds min(L=%d, 8)", fn, T, c->L);
-        rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
+        rc = check_activations(fn, q, k, v, a, rule == gdn::RULE_GDN ? b : a, in_dtype, A_log, dt_bias, out,
+                               out_dtype);
         if (rc) return rc;
+        if (rule == gdn::RULE_MAMBA2 && (!D || !aligned_to(D, 4)))
+            return fail(D ? GDN_ERR_ALIGN : GDN_ERR_NULL, "%s: D is NULL or misaligned", fn);
         if (in_dtype != c->ring_dtype)
             return fail(GDN_ERR_DTYPE, "%s: in_dtype=%d differs from the ring dtype %d", fn, in_dtype, c->ring_dtype);
     } else if (T < 0) {
@@ -107,6 +112,7 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
         return fail(GDN_ERR_ALIGN, "%s: cache arrays must be 16-byte aligned", fn);
 
     if (c->ckpt_read) {
+        if (rule != gdn::RULE_GDN) return fail(GDN_ERR_DTYPE, "%s: a read copy is not supported for Mamba2", fn);
         if (c->ckpt_dtype != GDN_F32 || (c->read_dtype != GDN_BF16 && c->read_dtype != GDN_F16))
             return fail(GDN_ERR_DTYPE, "%s: a read copy needs an fp32 checkpoint and a bf16/fp16 copy (ckpt=%d read=%d)", fn,
                         c->ckpt_dtype, c->read_dtype);
@@ -116,7 +122,7 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
     gdn::ReplayArgs p{};
     p.ckpt = c->ckpt, p.ring_k = c->ring_k, p.ring_v = c->ring_v, p.ring_rec = c->ring_rec;
     p.pos = c->pos, p.ckpt_pos = c->ckpt_pos, p.slots = slots;
-    p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias;
+    p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias, p.D = D;
     p.out = out, p.dev_err = dev_err;
     p.num_slots = dims->num_slots;
     p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.L = c->L, p.T = T, p.force = force != 0;
@@ -135,6 +141,15 @@ int replay_common(const char* fn, const gdn_dims* dims, const gdn_replay_cache* 
         p.mnchunk = dims->dv / p.mrows;
         e = c->read_dtype == GDN_BF16 ? gdn::dispatch_replay_f32_bf16(dims->dk, tmax, p, s, too_big)
                                       : gdn::dispatch_replay_f32_f16(dims->dk, tmax, p, s, too_big);
+    } else if (rule == gdn::RULE_MAMBA2) {
+        chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
+        p.mrows = p.rows, p.mnchunk = p.nchunk;
+        if (c->ckpt_dtype == GDN_F32)
+            e = gdn::dispatch_mamba2_replay_f32(dims->dk, tmax, p, s, too_big);
+        else if (c->ckpt_dtype == GDN_BF16)
+            e = gdn::dispatch_mamba2_replay_bf16(dims->dk, tmax, p, s, too_big);
+        else
+            e = gdn::dispatch_mamba2_replay_f16(dims->dk, tmax, p, s, too_big);
     } else {
         chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
         p.mrows = p.rows, p.mnchunk = p.nchunk;
@@ -219,8 +234,8 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
 int gdn_replay_step(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* q,
                     const void* k, const void* v, const void* a, const void* b, int32_t in_dtype, const float* A_log,
                     const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {
-    return replay_common("gdn_replay_step", dims, cache, slots, 1, 0, q, k, v, a, b, in_dtype, A_log, dt_bias, out,
-                         out_dtype, dev_err, stream);
+    return replay_common("gdn_replay_step", gdn::RULE_GDN, dims, cache, slots, 1, 0, q, k, v, a, b, in_dtype, A_log,
+                         dt_bias, nullptr, out, out_dtype, dev_err, stream);
 }
 
 int gdn_verify_window(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t T,
@@ -228,14 +243,15 @@ int gdn_verify_window(const gdn_dims* dims, const gdn_replay_cache* cache, const
                       const float* A_log, const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err,
                       void* stream) {
     if (T < 1) return fail(GDN_ERR_WINDOW, "gdn_verify_window: T=%d must be >= 1", T);
-    return replay_common("gdn_verify_window", dims, cache, slots, T, 0, q, k, v, a, b, in_dtype, A_log, dt_bias, out,
-                         out_dtype, dev_err, stream);
+    return replay_common("gdn_verify_window", gdn::RULE_GDN, dims, cache, slots, T, 0, q, k, v, a, b, in_dtype,
+                         A_log, dt_bias, nullptr, out, out_dtype, dev_err, stream);
 }
 
 int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t force,
                      int32_t* dev_err, void* stream) {
-    return replay_common("gdn_replay_flush", dims, cache, slots, 0, force, nullptr, nullptr, nullptr, nullptr, nullptr,
-                         cache ? cache->ring_dtype : GDN_F32, nullptr, nullptr, nullptr, GDN_F32, dev_err, stream);
+    return replay_common("gdn_replay_flush", gdn::RULE_GDN, dims, cache, slots, 0, force, nullptr, nullptr, nullptr,
+                         nullptr, nullptr, cache ? cache->ring_dtype : GDN_F32, nullptr, nullptr, nullptr, nullptr,
+                         GDN_F32, dev_err, stream);
 }
 
 int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const int32_t* accepted,
@@ -252,6 +268,89 @@ int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int3
     return launched(gdn::launch_rollback(cache->pos, cache->ckpt_pos, slots, accepted, dims->B, dims->Hv, T,
                                          dims->num_slots, dev_err, static_cast<cudaStream_t>(stream)),
                     fn);
+}
+
+// ---------------------------------------------------------------- Mamba2
+
+}  // extern "C"
+
+namespace {
+
+int m2_dims(const mamba2_dims* m, gdn_dims& d, const char* fn) {
+    if (!m) return fail(GDN_ERR_NULL, "%s: dims is NULL", fn);
+    d.B = m->B, d.Hk = m->G, d.Hv = m->H, d.dk = m->N, d.dv = m->P, d.num_slots = m->num_slots;
+    return check_dims(&d, fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mamba2_decode_step(const mamba2_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* slots,
+                       const void* x, const void* dt, const void* Bm, const void* Cm, int32_t in_dtype,
+                       const float* A_log, const float* dt_bias, const float* D, void* out, int32_t out_dtype,
+                       int32_t* dev_err, void* stream) {
+    const char* fn = "mamba2_decode_step";
+    gdn_dims d;
+    int rc = m2_dims(dims, d, fn);
+    if (rc) return rc;
+    if (d.B == 0) return GDN_OK;
+    if (!state_pool || !slots || !dev_err) return fail(GDN_ERR_NULL, "%s: state_pool, slots or dev_err is NULL", fn);
+    if (!dtype_ok(state_dtype)) return fail(GDN_ERR_DTYPE, "%s: unsupported state dtype %d", fn, state_dtype);
+    rc = check_activations(fn, Cm, Bm, x, dt, dt, in_dtype, A_log, dt_bias, out, out_dtype);
+    if (rc) return rc;
+    if (!D) return fail(GDN_ERR_NULL, "%s: D is NULL", fn);
+    if (!aligned16(state_pool) || !aligned_to(slots, 4) || !aligned_to(dev_err, 4) || !aligned_to(D, 4))
+        return fail(GDN_ERR_ALIGN, "%s: state_pool must be 16-byte aligned", fn);
+    gdn::DecodeArgs p{};
+    p.pool = state_pool, p.slots = slots, p.q = Cm, p.k = Bm, p.v = x, p.a = dt, p.b = nullptr;
+    p.A_log = A_log, p.dt_bias = dt_bias, p.D = D, p.out = out, p.dev_err = dev_err;
+    p.num_slots = d.num_slots;
+    p.B = d.B, p.Hk = d.Hk, p.Hv = d.Hv, p.dv = d.dv;
+    p.in_dtype = in_dtype, p.out_dtype = out_dtype;
+    p.q_scale = 1.f;
+    chunking(d.dk, d.dv, gdn::dtype_size(state_dtype), p.rows, p.nchunk);
+    return launched(gdn::dispatch_mamba2_decode(state_dtype, d.dk, p, static_cast<cudaStream_t>(stream)), fn);
+}
+
+int mamba2_verify_window(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t T,
+                         const void* x, const void* dt, const void* Bm, const void* Cm, int32_t in_dtype,
+                         const float* A_log, const float* dt_bias, const float* D, void* out, int32_t out_dtype,
+                         int32_t* dev_err, void* stream) {
+    const char* fn = T == 1 ? "mamba2_replay_step" : "mamba2_verify_window";
+    if (T < 1) return fail(GDN_ERR_WINDOW, "%s: T=%d must be >= 1", fn, T);
+    gdn_dims d;
+    int rc = m2_dims(dims, d, fn);
+    if (rc) return rc;
+    return replay_common(fn, gdn::RULE_MAMBA2, &d, cache, slots, T, 0, Cm, Bm, x, dt, nullptr, in_dtype, A_log,
+                         dt_bias, D, out, out_dtype, dev_err, stream);
+}
+
+int mamba2_replay_step(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* x,
+                       const void* dt, const void* Bm, const void* Cm, int32_t in_dtype, const float* A_log,
+                       const float* dt_bias, const float* D, void* out, int32_t out_dtype, int32_t* dev_err,
+                       void* stream) {
+    return mamba2_verify_window(dims, cache, slots, 1, x, dt, Bm, Cm, in_dtype, A_log, dt_bias, D, out, out_dtype,
+                                dev_err, stream);
+}
+
+int mamba2_replay_flush(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t force,
+                        int32_t* dev_err, void* stream) {
+    const char* fn = "mamba2_replay_flush";
+    gdn_dims d;
+    int rc = m2_dims(dims, d, fn);
+    if (rc) return rc;
+    return replay_common(fn, gdn::RULE_MAMBA2, &d, cache, slots, 0, force, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, cache ? cache->ring_dtype : GDN_F32, nullptr, nullptr, nullptr, nullptr, GDN_F32,
+                         dev_err, stream);
+}
+
+int mamba2_rollback(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                    const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream) {
+    gdn_dims d;
+    int rc = m2_dims(dims, d, "mamba2_rollback");
+    if (rc) return rc;
+    return gdn_rollback(&d, cache, slots, accepted, T, dev_err, stream);
 }
 
 const char* gdn_last_error_string(void) { return g_last_error.c_str(); }

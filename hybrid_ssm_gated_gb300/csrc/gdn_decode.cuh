@@ -29,6 +29,9 @@
 //    group's units. Every warp still waits for and releases every chunk in
 //    order, so no parity wait can alias.
 //  - Every wait is bounded (GDN_DEVERR_TIMEOUT, then return).
+// The same kernel runs the Mamba2 decode step (RULE_MAMBA2, gdn_device.cuh):
+// k, q and v rows carry B, C and x, nothing is normalised, delta_j = beta x_j
+// (beta being Mamba2's softplus step size), and o_j gains D x_j.
 #pragma once
 
 #include "gdn_device.cuh"
@@ -45,6 +48,7 @@ struct DecodeArgs {
     const void* b;
     const float* A_log;
     const float* dt_bias;
+    const float* D;  // Mamba2 skip weights [Hv]; unused by the gated delta rule
     void* out;
     int32_t* dev_err;
     int64_t num_slots;
@@ -85,7 +89,7 @@ struct DecodeCfg {
     static_assert(DK % E == 0 && LPR <= 32, "dk must be a multiple of 16 and at most 512");
 };
 
-template <typename ST, int DK, int NCW, int NS, int NH>
+template <typename ST, int DK, int NCW, int NS, int NH, int RULE = RULE_GDN>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeArgs p) {
     using C = DecodeCfg<ST, DK, NCW, NS, NH>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
             // lane l fetches the slot and gates of unit n0 + l
             const int my_unit = blockIdx.x + (n0 + lane) * gridDim.x;
             int slot = -1;
-            float alpha = 0.f, beta = 0.f;
+            float alpha = 0.f, beta = 0.f, dskip = 0.f;
             if (my_unit < total) {
                 const int b = my_unit / p.Hv, h = my_unit - b * p.Hv;
                 const int s = p.slots[b];
@@ -130,8 +134,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     set_error(p.dev_err, GDN_DEVERR_SLOT);
                 } else if (s >= 0) {
                     slot = s;
-                    gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, my_unit, p.in_dtype),
-                          load_elem(p.b, my_unit, p.in_dtype), alpha, beta);
+                    rule_gates<RULE>(p.A_log[h], p.dt_bias[h], p.a, p.b, my_unit, p.in_dtype, alpha, beta);
+                    if constexpr (RULE == RULE_MAMBA2) dskip = p.D[h];
                 }
             }
             for (int i = 0; i < 32; ++i, ++n) {
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                 const int s_i = __shfl_sync(FULL_MASK, slot, i);
                 const float al = __shfl_sync(FULL_MASK, alpha, i);
                 const float be = __shfl_sync(FULL_MASK, beta, i);
+                const float dsk = RULE == RULE_MAMBA2 ? __shfl_sync(FULL_MASK, dskip, i) : 0.f;
                 // A single thread issues a bulk copy only every ~0.25 us, so the unit's
                 // copies are spread over lanes: lanes 0-2 the q/k/v rows, lane c chunk c.
                 const int hs = n % NH;
@@ -150,6 +155,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                         reinterpret_cast<int*>(head)[0] = s_i;
                         reinterpret_cast<float*>(head)[1] = al;
                         reinterpret_cast<float*>(head)[2] = be;
+                        if constexpr (RULE == RULE_MAMBA2) reinterpret_cast<float*>(head)[3] = dsk;
                         if (s_i >= 0)
                             mbar_arrive_expect_tx(&hfull[hs], 2 * qbytes + vbytes);
                         else
@@ -217,6 +223,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
         const int slot = reinterpret_cast<const int*>(head)[0];
         const float alpha = reinterpret_cast<const float*>(head)[1];
         const float beta = reinterpret_cast<const float*>(head)[2];
+        const float dskip = reinterpret_cast<const float*>(head)[3];  // Mamba2's D[h]
         if (slot < 0) {
             for (int j = cw * 32 + lane; j < p.dv; j += NCW * 32)
                 store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, 0.f);
@@ -243,13 +250,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     kn2[e] = make_float2(kn[2 * e], kn[2 * e + 1]), qn2[e] = make_float2(qn[2 * e], qn[2 * e + 1]);
                     sk = __ffma2_rn(kn2[e], kn2[e], sk), sq = __ffma2_rn(qn2[e], qn2[e], sq);
                 }
-                const float ik = rsqrtf(group_sum<C::LPR>(sk.x + sk.y) + 1e-6f);
-                const float iq = rsqrtf(group_sum<C::LPR>(sq.x + sq.y) + 1e-6f) * p.q_scale;
+                // Mamba2 takes B and C as they are
+                const float ik = RULE == RULE_GDN ? rsqrtf(group_sum<C::LPR>(sk.x + sk.y) + 1e-6f) : 1.f;
+                const float iq = RULE == RULE_GDN ? rsqrtf(group_sum<C::LPR>(sq.x + sq.y) + 1e-6f) * p.q_scale : 1.f;
                 const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
                 float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int e = 0; e < C::E / 2; ++e) {
-                    kn2[e] = __fmul2_rn(kn2[e], ik2), qn2[e] = __fmul2_rn(qn2[e], iq2);
+                    if constexpr (RULE == RULE_GDN) kn2[e] = __fmul2_rn(kn2[e], ik2), qn2[e] = __fmul2_rn(qn2[e], iq2);
                     d2 = __ffma2_rn(kn2[e], qn2[e], d2);
                 }
                 qk = group_sum<C::LPR>(d2.x + d2.y);
@@ -280,13 +288,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
 #pragma unroll
                     for (int e = 0; e < C::E / 2; ++e) {
                         const float2 s2 = make_float2(s[2 * e], s[2 * e + 1]);
-                        u2 = __ffma2_rn(s2, kn2[e], u2);
+                        if constexpr (RULE == RULE_GDN) u2 = __ffma2_rn(s2, kn2[e], u2);
                         p2 = __ffma2_rn(s2, qn2[e], p2);
                     }
-                    const float u = group_sum<C::LPR>(u2.x + u2.y);
+                    const float u = RULE == RULE_GDN ? group_sum<C::LPR>(u2.x + u2.y) : 0.f;
                     const float pq = group_sum<C::LPR>(p2.x + p2.y);
                     const float vj = load_elem(head + C::OFF_V, j, p.in_dtype);
-                    const float delta = beta * (vj - alpha * u);
+                    const float delta = RULE == RULE_GDN ? beta * (vj - alpha * u) : beta * vj;
                     const float2 al2 = make_float2(alpha, alpha), d2 = make_float2(delta, delta);
 #pragma unroll
                     for (int e = 0; e < C::E / 2; ++e) {
@@ -297,8 +305,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
 #pragma unroll
                     for (int cc = 0; cc < C::NC; ++cc)
                         *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = Store<ST>::pack(s + cc * C::VEC);
-                    if (pg == 0)
-                        store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, fmaf(alpha, pq, qk * delta));
+                    if (pg == 0) {
+                        float o = fmaf(alpha, pq, qk * delta);
+                        if constexpr (RULE == RULE_MAMBA2) o = fmaf(dskip, vj, o);
+                        store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, o);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&cempty[cs]);

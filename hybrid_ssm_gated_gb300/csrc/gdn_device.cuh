@@ -289,6 +289,27 @@ __device__ __forceinline__ void gates(float A_log, float dt_bias, float a, float
     beta = 1.f / (1.f + expf(-b));
 }
 
+// The recurrence a kernel runs. GDN: the gated delta rule above. MAMBA2: the
+// Mamba2 decode recurrence with the same state layout (key = B, value = x,
+// query = C; no normalisation, no prediction term, plus the skip term D x):
+//   delta = softplus(dt + dt_bias),  alpha = exp(-exp(A_log) delta)
+//   S_t = alpha S_{t-1} + delta B x^T,   y_t = S_t^T C + D x
+enum Rule : int { RULE_GDN = 0, RULE_MAMBA2 = 1 };
+
+// Gates of one (sequence, head): GDN takes (a, b); Mamba2 takes dt in `a` and
+// returns delta in `beta`.
+template <int RULE>
+__device__ __forceinline__ void rule_gates(float A_log, float dt_bias, const void* a, const void* b, int64_t i,
+                                           int dt, float& alpha, float& beta) {
+    if constexpr (RULE == RULE_GDN) {
+        gates(A_log, dt_bias, load_elem(a, i, dt), load_elem(b, i, dt), alpha, beta);
+    } else {
+        const float x = load_elem(a, i, dt) + dt_bias;
+        beta = x > 20.f ? x : log1pf(expf(x));
+        alpha = expf(-expf(A_log) * beta);
+    }
+}
+
 __device__ __forceinline__ void set_error(int32_t* dev_err, int bits) { atomicOr(dev_err, bits); }
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }

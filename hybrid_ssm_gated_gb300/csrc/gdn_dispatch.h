@@ -22,6 +22,12 @@ cudaError_t dispatch_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t st
 cudaError_t dispatch_replay_f32_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_replay_f32_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
 
+// Mamba2 (RULE_MAMBA2): decode, and replay with one checkpoint (tmax in {1, 4, 8}).
+cudaError_t dispatch_mamba2_decode(int state_dtype, int dk, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t dispatch_mamba2_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_mamba2_replay_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+cudaError_t dispatch_mamba2_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStream_t stream, bool& too_big);
+
 // tmax in {4, 8}. too_big is set when the layout does not fit in shared memory.
 cudaError_t dispatch_spec_f32(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_spec_bf16(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);

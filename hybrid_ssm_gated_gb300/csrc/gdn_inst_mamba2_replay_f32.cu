@@ -1,0 +1,22 @@
+// Instantiations of the replay kernel for the Mamba2 recurrence, f32
+// checkpoints (d_state x window size).
+#include "gdn_dispatch.h"
+#include "gdn_launch_replay.cuh"
+
+namespace gdn {
+
+cudaError_t dispatch_mamba2_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t s, bool& too_big) {
+#define GDN_REP(DK)                                                                          \
+    if (dk == DK) {                                                                          \
+        if (tmax == 1) return launch_replay<float, DK, 1, float, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 4) return launch_replay<float, DK, 4, float, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 8) return launch_replay<float, DK, 8, float, RULE_MAMBA2>(a, s, too_big);    \
+    }
+    GDN_REP(32)
+    GDN_REP(64)
+    GDN_REP(128)
+#undef GDN_REP
+    return cudaErrorNotSupported;
+}
+
+}  // namespace gdn

@@ -93,11 +93,11 @@ constexpr int decode_stages() {
     return sizeof(ST) == 4 ? GDN_DECODE_CHUNK_STAGES : GDN_DECODE_CHUNK_STAGES_NARROW;
 }
 
-template <typename ST, int DK>
+template <typename ST, int DK, int RULE = RULE_GDN>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int NS = decode_stages<ST>();
     using C = DecodeCfg<ST, DK, DEC_NCW, NS, DEC_NH>;
-    auto kern = decode_kernel<ST, DK, DEC_NCW, NS, DEC_NH>;
+    auto kern = decode_kernel<ST, DK, DEC_NCW, NS, DEC_NH, RULE>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;

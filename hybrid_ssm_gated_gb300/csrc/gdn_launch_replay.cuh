@@ -65,12 +65,13 @@ int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
     return total(ns, nh);
 }
 
-// ST: the checkpoint steps read; MT: the one folds update (a wider master, or ST).
-template <typename ST, int DK, int TMAX, typename MT = ST>
+// ST: the checkpoint steps read; MT: the one folds update (a wider master, or ST);
+// RULE: the recurrence (gated delta rule or Mamba2).
+template <typename ST, int DK, int TMAX, typename MT = ST, int RULE = RULE_GDN>
 cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
     constexpr int NCW = replay_warps<TMAX>();
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
-    auto kern = replay_kernel<ST, DK, TMAX, NCW, MT>;
+    auto kern = replay_kernel<ST, DK, TMAX, NCW, MT, RULE>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;

@@ -54,6 +54,10 @@
 // rewrites the copy from the stored rows; the call's tokens then continue
 // from the copy's values, as if it had been read back. A master chunk holds
 // fewer rows, so its items release the chunk with a larger weight.
+// Mamba2 (RULE_MAMBA2, gdn_device.cuh) runs through the same kernel: keys,
+// queries and values are B, C and x, nothing is normalised (the stored inverse
+// key norm is 1), w_e = delta_e x_e needs no prediction, so the S^T k sums and
+// their ring terms are skipped, and every output gains D x.
 // Hand-offs. Every warp visits every head stage in order, so the head and
 // table barriers' parity waits cannot alias. The head barrier takes two
 // arrivals: one arms its copies, the other comes with the metadata once every
@@ -90,6 +94,7 @@ struct ReplayArgs {
     const void* b;
     const float* A_log;
     const float* dt_bias;
+    const float* D;  // Mamba2 skip weights [Hv]; unused by the gated delta rule
     void* out;
     int32_t* dev_err;
     int64_t num_slots;
@@ -210,7 +215,7 @@ __device__ __forceinline__ void reduce_scatter_values(float (&x)[V], int g) {
 
 // ST: the checkpoint that steps and windows read (the read copy in the two-checkpoint mode);
 // MT: the checkpoint that folds read and write (ST itself with one checkpoint).
-template <typename ST, int DK, int TMAX, int NCW, typename MT = ST>
+template <typename ST, int DK, int TMAX, int NCW, typename MT = ST, int RULE = RULE_GDN>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayArgs p) {
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
     constexpr bool MIXED = !std::is_same<ST, MT>::value;
@@ -285,8 +290,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         for (int t = 0; t < TMAX; ++t) {
                             if (t < T) {
                                 const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
-                                gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
-                                      load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
+                                rule_gates<RULE>(p.A_log[h], p.dt_bias[h], p.a, p.b, gi, p.in_dtype, al[t], be[t]);
                             }
                         }
                     } else {
@@ -497,14 +501,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         load_run<C::VEC>(head + p.off_wk + t * DK * in_sz, pos_of(cc), p.in_dtype, xk + cc * C::VEC);
                         load_run<C::VEC>(head + p.off_wq + t * DK * in_sz, pos_of(cc), p.in_dtype, xq + cc * C::VEC);
                     }
-                    float ssk = 0.f, ssq = 0.f;
+                    ikw[t] = 1.f;
+                    if constexpr (RULE == RULE_GDN) {
+                        float ssk = 0.f, ssq = 0.f;
 #pragma unroll
-                    for (int e = 0; e < C::E; ++e) ssk = fmaf(xk[e], xk[e], ssk), ssq = fmaf(xq[e], xq[e], ssq);
-                    const float ik = rsqrtf(group_sum<C::LPR>(ssk) + 1e-6f);
-                    const float iq = rsqrtf(group_sum<C::LPR>(ssq) + 1e-6f) * p.q_scale;
-                    ikw[t] = ik;
+                        for (int e = 0; e < C::E; ++e) ssk = fmaf(xk[e], xk[e], ssk), ssq = fmaf(xq[e], xq[e], ssq);
+                        const float ik = rsqrtf(group_sum<C::LPR>(ssk) + 1e-6f);
+                        const float iq = rsqrtf(group_sum<C::LPR>(ssq) + 1e-6f) * p.q_scale;
+                        ikw[t] = ik;
 #pragma unroll
-                    for (int e = 0; e < C::E; ++e) xk[e] *= ik, xq[e] *= iq;
+                        for (int e = 0; e < C::E; ++e) xk[e] *= ik, xq[e] *= iq;
+                    }
                 }
 #pragma unroll
                 for (int e = 0; e < C::E / 2; ++e)
@@ -556,7 +563,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         float2 a2 = make_float2(0.f, 0.f), b2 = a2;
 #pragma unroll
                         for (int e = 0; e < C::E / 2; ++e)
-                            a2 = __ffma2_rn(kx[e], kw2[t][e], a2), b2 = __ffma2_rn(kx[e], qw2[t][e], b2);
+                        {
+                            if constexpr (RULE == RULE_GDN) a2 = __ffma2_rn(kx[e], kw2[t][e], a2);
+                            b2 = __ffma2_rn(kx[e], qw2[t][e], b2);
+                        }
                         v[t] = a2.x + a2.y;
                         v[TMAX + t] = b2.x + b2.y;
                     }
@@ -617,6 +627,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
             }
 
             if (rows_here) {
+                // Mamba2's skip weight (a flush, T = 0, has no outputs and no D)
+                const float dskip = RULE == RULE_MAMBA2 && T > 0 ? p.D[h] : 0.f;
                 const float g1 = fold ? 1.f : gring;  // decay of S0 to the window's first token
                 // fold: scale of entry f's rank-one term, R(f) / |k_f| (lane f)
                 const float fsc = lane < count ? R * rec[lane * rec_floats + 2] : 0.f;
@@ -732,17 +744,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
 #pragma unroll
                                     for (int e = 0; e < C::E / 2; ++e) {
                                         const float2 s2 = make_float2(s[r][2 * e], s[r][2 * e + 1]);
-                                        u2 = __ffma2_rn(s2, kw2[0][e], u2);
+                                        if constexpr (RULE == RULE_GDN) u2 = __ffma2_rn(s2, kw2[0][e], u2);
                                         v2 = __ffma2_rn(s2, qw2[0][e], v2);
                                     }
                                     // after a fold the window's first token follows S0 directly
                                     const float Y = group_sum<C::LPR>(u2.x + u2.y);
                                     const float Z = group_sum<C::LPR>(v2.x + v2.y) * al;
                                     const int j = jr[r];
-                                    const float ww = be * (load_elem(head + p.off_wv, j, p.in_dtype) - al * Y);
+                                    const float vj = load_elem(head + p.off_wv, j, p.in_dtype);
+                                    const float ww = RULE == RULE_GDN ? be * (vj - al * Y) : be * vj;
                                     if (pg == 0) {
                                         store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype,
-                                                   fmaf(qk, ww, Z));
+                                                   fmaf(dskip, vj, fmaf(qk, ww, Z)));
                                         p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                                     }
                                 }
@@ -769,7 +782,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
 #pragma unroll
                                     for (int e = 0; e < C::VEC / 2; ++e) {
                                         const float2 s2 = make_float2(sv[2 * e], sv[2 * e + 1]);
-                                        u2[ps] = __ffma2_rn(s2, kw2[0][cc * C::VEC / 2 + e], u2[ps]);
+                                        if constexpr (RULE == RULE_GDN)
+                                            u2[ps] = __ffma2_rn(s2, kw2[0][cc * C::VEC / 2 + e], u2[ps]);
                                         v2[ps] = __ffma2_rn(s2, qw2[0][cc * C::VEC / 2 + e], v2[ps]);
                                     }
                                 }
@@ -782,7 +796,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         if (lane == 0) mbar_arrive_n(&cempty[cs], C::SUB);
                         if (T > 0) {
                             const float al = meta->alpha[0], be = meta->beta[0];
-                            float Y = reduce_scatter<C::PPI>(y, pg) * g1;
+                            float Y = RULE == RULE_GDN ? reduce_scatter<C::PPI>(y, pg) * g1 : 0.f;
                             float Z = reduce_scatter<C::PPI>(z, pg) * (g1 * al);
                             const int j = j0 + pg * C::RPP + rsub;
                             if (cpr > 0) {
@@ -794,19 +808,21 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 for (; f + 2 <= cpr; f += 2) {
                                     const float2 c0 = cf2[f], c1 = cf2[f + 1];
                                     const float w0 = rec[f * rec_floats + 4 + j], w1 = rec[(f + 1) * rec_floats + 4 + j];
-                                    Y = fmaf(c0.x, w0, Y), Z = fmaf(c0.y, w0, Z);
-                                    Y1 = fmaf(c1.x, w1, Y1), Z1 = fmaf(c1.y, w1, Z1);
+                                    Z = fmaf(c0.y, w0, Z), Z1 = fmaf(c1.y, w1, Z1);
+                                    if constexpr (RULE == RULE_GDN) Y = fmaf(c0.x, w0, Y), Y1 = fmaf(c1.x, w1, Y1);
                                 }
                                 if (f < cpr) {
                                     const float2 c0 = cf2[f];
                                     const float w0 = rec[f * rec_floats + 4 + j];
-                                    Y = fmaf(c0.x, w0, Y), Z = fmaf(c0.y, w0, Z);
+                                    Z = fmaf(c0.y, w0, Z);
+                                    if constexpr (RULE == RULE_GDN) Y = fmaf(c0.x, w0, Y);
                                 }
                                 Y += Y1, Z += Z1;
                             }
                             const float vj = load_elem(head + p.off_wv, j, p.in_dtype);
-                            const float ww = be * (vj - al * Y);
-                            store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype, fmaf(qk, ww, Z));
+                            const float ww = RULE == RULE_GDN ? be * (vj - al * Y) : be * vj;
+                            store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype,
+                                       fmaf(dskip, vj, fmaf(qk, ww, Z)));
                             p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                         }
                     } else {
@@ -838,7 +854,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
 #pragma unroll
                                     for (int e = 0; e < C::E / 2; ++e) {
                                         const float2 x2 = make_float2(s2[r][2 * e], s2[r][2 * e + 1]);
-                                        a2 = __ffma2_rn(x2, kw2[t][e], a2);
+                                        if constexpr (RULE == RULE_GDN) a2 = __ffma2_rn(x2, kw2[t][e], a2);
                                         b2 = __ffma2_rn(x2, qw2[t][e], b2);
                                     }
                                     v[r][t] = (a2.x + a2.y) * G1;
@@ -883,7 +899,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                             for (int x = 0; x < TMAX; ++x) {
                                 if (x < T) {
                                     const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, p.in_dtype);
-                                    const float wx = meta->beta[x] * (vx - meta->alpha[x] * y[x]);
+                                    const float wx = RULE == RULE_GDN ? meta->beta[x] * (vx - meta->alpha[x] * y[x])
+                                                                      : meta->beta[x] * vx;
                                     wcol[(int64_t)ri * rec_floats] = wx;
                                     if (++ri == L) ri = 0;
                                     const float* cx = coef + (cpr + x) * C::V;
@@ -896,7 +913,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                             const int64_t ot = (int64_t)p.Hv * p.dv;                    // next token
 #pragma unroll
                             for (int t = 0; t < TMAX; ++t)
-                                if (t < T) store_elem(p.out, ob + t * ot, p.out_dtype, z[t]);
+                                if (t < T) {
+                                    float o = z[t];
+                                    if constexpr (RULE == RULE_MAMBA2)
+                                        o = fmaf(dskip, load_elem(head + p.off_wv + t * p.dv * in_sz, j, p.in_dtype), o);
+                                    store_elem(p.out, ob + t * ot, p.out_dtype, o);
+                                }
                         }
                         __syncwarp();  // the tile is free for the next item
                     }

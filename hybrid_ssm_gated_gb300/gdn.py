@@ -41,6 +41,11 @@ class gdn_replay_cache(C.Structure):
                 ("ckpt_pos", C.c_void_p), ("L", C.c_int32), ("ckpt_read", C.c_void_p), ("read_dtype", C.c_int32)]
 
 
+class mamba2_dims(C.Structure):
+    _fields_ = [("B", C.c_int32), ("G", C.c_int32), ("H", C.c_int32), ("N", C.c_int32), ("P", C.c_int32),
+                ("num_slots", C.c_int64)]
+
+
 _lib = None
 _P = C.c_void_p
 _I = C.c_int32
@@ -53,6 +58,13 @@ _SIGS = {
                           _P, _I, _P, _P],
     "gdn_replay_flush": [C.POINTER(gdn_dims), C.POINTER(gdn_replay_cache), _P, _I, _P, _P],
     "gdn_rollback": [C.POINTER(gdn_dims), C.POINTER(gdn_replay_cache), _P, _P, _I, _P, _P],
+    "mamba2_decode_step": [C.POINTER(mamba2_dims), _P, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P],
+    "mamba2_replay_step": [C.POINTER(mamba2_dims), C.POINTER(gdn_replay_cache), _P, _P, _P, _P, _P, _I, _P, _P, _P,
+                           _P, _I, _P, _P],
+    "mamba2_verify_window": [C.POINTER(mamba2_dims), C.POINTER(gdn_replay_cache), _P, _I, _P, _P, _P, _P, _I, _P,
+                             _P, _P, _P, _I, _P, _P],
+    "mamba2_replay_flush": [C.POINTER(mamba2_dims), C.POINTER(gdn_replay_cache), _P, _I, _P, _P],
+    "mamba2_rollback": [C.POINTER(mamba2_dims), C.POINTER(gdn_replay_cache), _P, _P, _I, _P, _P],
 }
 
 
@@ -78,7 +90,8 @@ def declared_symbols() -> list[str]:
     """Names of the functions include/gdn.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gdn_[a-z_]+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*((?:gdn|mamba2)_[a-z_0-9]+)\s*\(", text,
+                                 re.M)))
 
 
 def gdn_last_error_string() -> str:
@@ -222,3 +235,63 @@ def gdn_rollback(cache: ReplayCache, slots, accepted, T: int, dev_err, stream=No
     cs = cache.c_struct()
     _check(lib().gdn_rollback(C.byref(d), C.byref(cs), _ptr(slots), _ptr(accepted), int(T), _ptr(dev_err),
                               _stream(stream)))
+
+
+# ---------------------------------------------------------------- Mamba2
+
+
+def _m2_dims(num_slots: int, H: int, P: int, N: int, B: int, G: int) -> mamba2_dims:
+    return mamba2_dims(B, G, H, N, P, num_slots)
+
+
+def mamba2_decode_step(state_pool, slots, x, dt, Bm, Cm, A_log, dt_bias, D, out, dev_err, stream=None) -> None:
+    """Mamba2 decode step: state_pool [num_slots, H, P, N]; slots [B] int32; x [B, H, P]; dt [B, H];
+    Bm, Cm [B, G, N]; A_log, dt_bias, D [H] fp32; out [B, H, P]; dev_err [1] int32."""
+    num_slots, H, P, N = state_pool.shape
+    d = _m2_dims(num_slots, H, P, N, slots.shape[0], Bm.shape[-2])
+    _check(lib().mamba2_decode_step(C.byref(d), _ptr(state_pool), _code(state_pool), _ptr(slots), _ptr(x), _ptr(dt),
+                                    _ptr(Bm), _ptr(Cm), _code(x), _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(out),
+                                    _code(out), _ptr(dev_err), _stream(stream)))
+
+
+def _m2_replay_dims(cache: ReplayCache, slots, Bm) -> mamba2_dims:
+    num_slots, H, P, N = cache.shape
+    return _m2_dims(num_slots, H, P, N, slots.shape[0], Bm.shape[-2] if Bm is not None else H)
+
+
+def mamba2_replay_step(cache: ReplayCache, slots, x, dt, Bm, Cm, A_log, dt_bias, D, out, dev_err,
+                       stream=None) -> None:
+    """One Mamba2 ReplaySSM step; arguments shaped as for mamba2_decode_step."""
+    d = _m2_replay_dims(cache, slots, Bm)
+    cs = cache.c_struct()
+    _check(lib().mamba2_replay_step(C.byref(d), C.byref(cs), _ptr(slots), _ptr(x), _ptr(dt), _ptr(Bm), _ptr(Cm),
+                                    _code(x), _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(out), _code(out),
+                                    _ptr(dev_err), _stream(stream)))
+
+
+def mamba2_verify_window(cache: ReplayCache, slots, x, dt, Bm, Cm, A_log, dt_bias, D, out, dev_err,
+                         stream=None) -> None:
+    """A T-token Mamba2 verify window: x [B, T, H, P]; dt [B, T, H]; Bm, Cm [B, T, G, N];
+    out [B, T, H, P]."""
+    T = x.shape[1]
+    d = _m2_replay_dims(cache, slots, Bm)
+    cs = cache.c_struct()
+    _check(lib().mamba2_verify_window(C.byref(d), C.byref(cs), _ptr(slots), T, _ptr(x), _ptr(dt), _ptr(Bm),
+                                      _ptr(Cm), _code(x), _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(out),
+                                      _code(out), _ptr(dev_err), _stream(stream)))
+
+
+def mamba2_replay_flush(cache: ReplayCache, slots, force: bool, dev_err, stream=None) -> None:
+    """Fold Mamba2 rings into their checkpoints (full ones, or every non-empty one when force)."""
+    d = _m2_replay_dims(cache, slots, None)
+    cs = cache.c_struct()
+    _check(lib().mamba2_replay_flush(C.byref(d), C.byref(cs), _ptr(slots), int(bool(force)), _ptr(dev_err),
+                                     _stream(stream)))
+
+
+def mamba2_rollback(cache: ReplayCache, slots, accepted, T: int, dev_err, stream=None) -> None:
+    """Keep 1 + accepted[b] of the last Mamba2 verify window's T tokens (pointer move only)."""
+    d = _m2_replay_dims(cache, slots, None)
+    cs = cache.c_struct()
+    _check(lib().mamba2_rollback(C.byref(d), C.byref(cs), _ptr(slots), _ptr(accepted), int(T), _ptr(dev_err),
+                                 _stream(stream)))

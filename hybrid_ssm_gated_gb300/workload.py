@@ -12,6 +12,12 @@ Shapes and distributions follow the synthetic decode workloads of this
 library (Qwen3-Next-shaped GDN layers: Hk=16 key heads, Hv=32 value heads,
 dk=dv=128): q/k/v/a/b ~ N(0,1) in the input dtype, A_log ~ U(0,2),
 dt_bias ~ U(-1,1), initial states ~ N(0, 0.1) rounded to the state dtype.
+
+Mamba2 workloads reuse the same fields with Hk = groups G, Hv = heads H,
+dk = state dim N and dv = head dim P: x, dt, B, C ~ N(0,1) in the input dtype;
+A_log = ln U(1, 16), dt_bias = the softplus inverse of a step size drawn
+log-uniform in [0.001, 0.1], D ~ U(0.5, 1.5) (the ranges Mamba2 layers are
+initialised in).
 """
 from __future__ import annotations
 
@@ -25,7 +31,7 @@ DTYPE_CODE = {"f32": F32, "bf16": BF16, "f16": F16}
 DTYPE_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
 
 # Seed-stream tags: each kind of draw has its own stream.
-_TAG_PARAMS, _TAG_STATE, _TAG_STEP, _TAG_SLOTS, _TAG_OFFSETS, _TAG_ACCEPT = range(6)
+_TAG_PARAMS, _TAG_STATE, _TAG_STEP, _TAG_SLOTS, _TAG_OFFSETS, _TAG_ACCEPT, _TAG_M2_PARAMS, _TAG_M2_STEP = range(8)
 
 
 @dataclass(frozen=True)
@@ -85,6 +91,14 @@ WORKLOADS = {
                                 L=16, T=4),
     "verify_b256_bf16": Workload("verify_b256_bf16", B=256, Hk=16, Hv=32, dk=128, dv=128, steps=32,
                                  state_dtype="bf16", L=16, T=4),
+    # Mamba2 layer of 128 heads, head dim 64, state dim 128, 8 groups (Hk = G, Hv = H, dk = N, dv = P).
+    "mamba2_b256_f32": Workload("mamba2_b256_f32", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64),
+    "mamba2_b256_bf16": Workload("mamba2_b256_bf16", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64,
+                                 state_dtype="bf16"),
+    "mamba2_replay_b256_f32": Workload("mamba2_replay_b256_f32", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64,
+                                       L=16, max_offset=15),
+    "mamba2_replay_b256_bf16": Workload("mamba2_replay_b256_bf16", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64,
+                                        state_dtype="bf16", L=16, max_offset=15),
 }
 
 
@@ -189,3 +203,29 @@ def start_offsets(w: Workload) -> np.ndarray:
 def accepted(w: Workload, round_: int) -> np.ndarray:
     """Accepted draft tokens per sequence for one verify round, uniform in {0..T-1}."""
     return _rng(w, _TAG_ACCEPT, round_).integers(0, w.T, size=w.B).astype(np.int32)
+
+
+# ---------------------------------------------------------------- Mamba2 draws
+
+
+def mamba2_params(w: Workload) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """A_log = ln U(1, 16), dt_bias = softplus^-1(step) with step log-uniform in [0.001, 0.1],
+    D ~ U(0.5, 1.5); float32 [H]."""
+    r = _rng(w, _TAG_M2_PARAMS)
+    A_log = np.log(r.uniform(1.0, 16.0, size=w.Hv)).astype(np.float32)
+    step = np.exp(r.uniform(np.log(1e-3), np.log(1e-1), size=w.Hv))
+    dt_bias = (step + np.log(-np.expm1(-step))).astype(np.float32)
+    D = r.uniform(0.5, 1.5, size=w.Hv).astype(np.float32)
+    return A_log, dt_bias, D
+
+
+def mamba2_step_inputs(w: Workload, step: int) -> dict[str, np.ndarray]:
+    """Activations of one Mamba2 decode step (or a window of T tokens): x [B, T, H, P], dt [B, T, H],
+    Bm, Cm [B, T, G, N]; all ~ N(0,1) in the input dtype."""
+    r = _rng(w, _TAG_M2_STEP, step)
+    T = w.T
+    out = {}
+    for name, shape in (("x", (w.B, T, w.Hv, w.dv)), ("dt", (w.B, T, w.Hv)), ("Bm", (w.B, T, w.Hk, w.dk)),
+                        ("Cm", (w.B, T, w.Hk, w.dk))):
+        out[name] = quantize(r.standard_normal(shape, dtype=np.float32), w.in_dtype)
+    return out

@@ -45,6 +45,11 @@
  *   - Shapes: dk in {32, 64, 128}; dv a multiple of 16 in [16, 256] (of 32
  *     for the ReplaySSM entry points); Hv a multiple of Hk; B >= 0 (B == 0
  *     launches nothing).
+ *
+ * The same kernels also run the Mamba2 decode recurrence (entry points
+ * mamba2_*, at the end of this header), the other state-space layer the
+ * ReplaySSM article covers (section "每步写回完整循环状态": a state of shape
+ * (nheads, d, n) read through the vector C).
  */
 #ifndef GDN_H
 #define GDN_H
@@ -55,7 +60,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 2
+#define GDN_ABI_VERSION 3
 
 /* Host-side return codes. */
 #define GDN_OK 0
@@ -231,6 +236,65 @@ int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const 
  */
 int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
                  const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream);
+
+/*
+ * ---------------------------------------------------------------- Mamba2
+ *
+ * The Mamba2 decode recurrence (the standard one; the ReplaySSM article names
+ * its state shape (nheads, d, n) and its readout vector C, section "每步写回
+ * 完整循环状态"). Per sequence b and head h, group g = h / (H / G):
+ *     delta = softplus(dt[b,h] + dt_bias[h]),  alpha = exp(-exp(A_log[h]) delta)
+ *     S_t[p][i] = alpha S_{t-1}[p][i] + delta x[b,h][p] B[b,g][i]
+ *     y_t[p]    = sum_i S_t[p][i] C[b,g][i] + D[h] x[b,h][p]
+ * A head state is P rows of N contiguous elements, a pool [num_slots][H][P][N]
+ * -- the layout of a GDN pool with dk = N and dv = P. Activations: x [B][H][P],
+ * dt [B][H], Bm, Cm [B][G][N] in in_dtype; A_log, dt_bias, D fp32 [H]
+ * (A = -exp(A_log) is Mamba2's per-head decay rate). Shapes: N in
+ * {32, 64, 128}; P a multiple of 16 in [16, 256] (of 32 for replay); H a
+ * multiple of G. Conventions otherwise as above.
+ */
+typedef struct mamba2_dims {
+    int32_t B;          /* sequences in the batch */
+    int32_t G;          /* groups (rows of B and C per sequence) */
+    int32_t H;          /* heads */
+    int32_t N;          /* state dim (d_state) */
+    int32_t P;          /* head dim */
+    int64_t num_slots;  /* slots in the state pool / replay cache */
+} mamba2_dims;
+
+/* mamba2_decode_step -- one decode step: reads and writes pool[slots[b]]
+ * (rounded once to state_dtype), out [B][H][P] in out_dtype. */
+int mamba2_decode_step(const mamba2_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* slots,
+                       const void* x, const void* dt, const void* Bm, const void* Cm, int32_t in_dtype,
+                       const float* A_log, const float* dt_bias, const float* D, void* out, int32_t out_dtype,
+                       int32_t* dev_err, void* stream);
+
+/*
+ * Mamba2 ReplaySSM, on a gdn_replay_cache read as: ckpt [num_slots][H][P][N];
+ * ring_k [num_slots][H][L][N] the raw B rows; ring_v [num_slots][H][L][P] the
+ * raw x rows; ring_rec [num_slots][H][L][4 + P] fp32 = {alpha, delta, 1, 0,
+ * w[P] = delta x}; pos, ckpt_pos [num_slots][H]. C is never buffered (the
+ * ReplaySSM article: the readout vector comes from the current activations).
+ * Folding, windows and rollback follow the gdn_replay_* rules exactly; the
+ * read copy (ckpt_read) is not supported here (GDN_ERR_DTYPE).
+ *   mamba2_replay_step    one token: out [B][H][P].
+ *   mamba2_verify_window  T tokens, 1 <= T <= min(L, 8): x [B][T][H][P],
+ *                         dt [B][T][H], Bm, Cm [B][T][G][N], out [B][T][H][P].
+ *   mamba2_replay_flush   fold full rings (or non-empty ones with force).
+ *   mamba2_rollback       keep 1 + accepted[b] of the last window's T tokens.
+ */
+int mamba2_replay_step(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* x,
+                       const void* dt, const void* Bm, const void* Cm, int32_t in_dtype, const float* A_log,
+                       const float* dt_bias, const float* D, void* out, int32_t out_dtype, int32_t* dev_err,
+                       void* stream);
+int mamba2_verify_window(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, int32_t T,
+                         const void* x, const void* dt, const void* Bm, const void* Cm, int32_t in_dtype,
+                         const float* A_log, const float* dt_bias, const float* D, void* out, int32_t out_dtype,
+                         int32_t* dev_err, void* stream);
+int mamba2_replay_flush(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                        int32_t force, int32_t* dev_err, void* stream);
+int mamba2_rollback(const mamba2_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
+                    const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream);
 
 /* Text of the last host-side failure on the calling thread ("" if none). */
 const char* gdn_last_error_string(void);

@@ -26,7 +26,9 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = gdn.declared_symbols()
     assert set(names) >= {"gdn_decode_step", "gdn_replay_step", "gdn_replay_flush", "gdn_verify_window",
-                          "gdn_rollback", "gdn_last_error_string", "gdn_abi_version"}
+                          "gdn_rollback", "gdn_last_error_string", "gdn_abi_version", "gdn_spec_step",
+                          "mamba2_decode_step", "mamba2_replay_step", "mamba2_verify_window", "mamba2_replay_flush",
+                          "mamba2_rollback"}
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/gdn.h but not exported"
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.LIB_PATH], capture_output=True, text=True).stdout
@@ -35,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert gdn.gdn_abi_version() == 2
+    assert gdn.gdn_abi_version() == 3
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -44,7 +46,9 @@ def test_struct_layout_matches_header(tmp_path):
                    'printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(gdn_dims), offsetof(gdn_dims, num_slots),'
                    'sizeof(gdn_replay_cache), offsetof(gdn_replay_cache, ring_rec),'
                    'offsetof(gdn_replay_cache, ckpt_pos), offsetof(gdn_replay_cache, L),'
-                   'offsetof(gdn_replay_cache, ckpt_read), offsetof(gdn_replay_cache, read_dtype)); return 0;}\n')
+                   'offsetof(gdn_replay_cache, ckpt_read), offsetof(gdn_replay_cache, read_dtype));'
+                   'printf("%zu %zu %zu\\n", sizeof(mamba2_dims), offsetof(mamba2_dims, P),'
+                   'offsetof(mamba2_dims, num_slots)); return 0;}\n')
     exe = tmp_path / "layout"
     inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
     subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
@@ -52,7 +56,8 @@ def test_struct_layout_matches_header(tmp_path):
     want = [C.sizeof(gdn.gdn_dims), gdn.gdn_dims.num_slots.offset, C.sizeof(gdn.gdn_replay_cache),
             gdn.gdn_replay_cache.ring_rec.offset, gdn.gdn_replay_cache.ckpt_pos.offset,
             gdn.gdn_replay_cache.L.offset, gdn.gdn_replay_cache.ckpt_read.offset,
-            gdn.gdn_replay_cache.read_dtype.offset]
+            gdn.gdn_replay_cache.read_dtype.offset, C.sizeof(gdn.mamba2_dims), gdn.mamba2_dims.P.offset,
+            gdn.mamba2_dims.num_slots.offset]
     assert got == want
 
 
@@ -153,3 +158,42 @@ def test_spec_rejections(lib):
     assert _spec(lib, d, pool=FAKE + 8) == -5
     assert _spec(lib, d, q=FAKE + 4) == -5
     assert _spec(lib, _dims(B=0), pool=None, src=None, dst=None) == 0  # nothing to do, nothing touched
+
+
+def _m2dims(B=4, G=2, H=8, N=128, P=64, num_slots=8):
+    return gdn.mamba2_dims(B, G, H, N, P, num_slots)
+
+
+def _m2decode(lib, dims, pool=FAKE, sdt=0, x=FAKE, dt=FAKE, Bm=FAKE, Cm=FAKE, idt=1, D=FAKE, err=FAKE):
+    d = C.byref(dims) if dims is not None else None
+    return lib.mamba2_decode_step(d, pool, sdt, FAKE, x, dt, Bm, Cm, idt, FAKE, FAKE, D, FAKE, 0, err, None)
+
+
+def _m2verify(lib, dims, cache, T, D=FAKE, idt=1):
+    return lib.mamba2_verify_window(C.byref(dims), C.byref(cache), FAKE, T, FAKE, FAKE, FAKE, FAKE, idt, FAKE,
+                                    FAKE, D, FAKE, 0, FAKE, None)
+
+
+def test_mamba2_rejections(lib):
+    assert _m2decode(lib, None) == -1
+    assert _m2decode(lib, _m2dims(N=96)) == -3  # state dim not in {32, 64, 128}
+    assert _m2decode(lib, _m2dims(P=40)) == -3
+    assert _m2decode(lib, _m2dims(G=3, H=8)) == -3  # H not a multiple of G
+    assert _m2decode(lib, _m2dims(), D=None) == -1
+    assert _m2decode(lib, _m2dims(), dt=None) == -1
+    assert _m2decode(lib, _m2dims(), Cm=FAKE + 4) == -5
+    assert _m2decode(lib, _m2dims(), sdt=3) == -2
+    assert _m2decode(lib, _m2dims(B=0), pool=None) == 0
+    d = _m2dims()
+    assert _m2verify(lib, d, _cache(), 4, D=None) == -1
+    assert _m2verify(lib, d, _cache(), 4, D=FAKE + 2) == -5
+    assert _m2verify(lib, d, _cache(L=4), 5) == -4
+    assert _m2verify(lib, d, _cache(), 0) == -4
+    assert _m2verify(lib, _m2dims(P=48), _cache(), 4) == -3  # replay needs P % 32 == 0
+    assert _m2verify(lib, d, _cache(read=FAKE, read_dt=1), 4) == -2  # no read copy for Mamba2
+    assert "Mamba2" in gdn.gdn_last_error_string()
+    assert lib.mamba2_replay_step(C.byref(d), C.byref(_cache(rdt=0)), FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE,
+                                  FAKE, FAKE, 0, FAKE, None) == -2  # input dtype differs from the ring's
+    assert lib.mamba2_replay_flush(C.byref(_m2dims(N=48)), C.byref(_cache()), FAKE, 1, FAKE, None) == -3
+    assert lib.mamba2_rollback(C.byref(d), C.byref(_cache(L=4)), FAKE, FAKE, 5, FAKE, None) == -4
+    assert lib.mamba2_rollback(C.byref(_m2dims(B=0)), C.byref(_cache()), None, None, 4, None, None) == 0
