@@ -5,7 +5,8 @@ activations, fp32 state pool of 512 slots), and the decode kernel's achieved
 HBM bandwidth against the measured peak. One "step" is one decode step of the
 whole batch: gating, q/k normalisation, slot gather, fused update + readout,
 round + scatter -- all inside one kernel launch. The same JSON line also
-carries narrow-state decode, the ReplaySSM step and the T=4 verify window.
+carries narrow-state decode, the ReplaySSM step and the T=4 verify window,
+the speculative-step baseline, and a Mamba2 layer's decode and ReplaySSM step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -34,6 +35,8 @@ METRIC = "GDN decode tokens/s at B=256,Hv=32,d=128; achieved HBM GB/s vs GB300 p
 B, HK, HV, DK, DV = 256, 16, 32, 128, 128
 NUM_SLOTS = 2 * B
 L_RING, T_VERIFY = 16, 4
+# Mamba2 layer: groups, heads, state dim, head dim
+M2_G, M2_H, M2_N, M2_P = 8, 128, 128, 64
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gdn_decode.cuh", "gdn_device.cuh", "gdn_launch.cuh"]
 
@@ -67,6 +70,25 @@ def replay_unit_bytes(count: int, T: int, fold: bool, ckpt_bytes: int, in_bytes:
     inputs = T * (2 * DK * in_bytes * HK // HV + DV * in_bytes + 2 * in_bytes)
     return (state + count * (DK * in_bytes + rec) + inputs + T * (DK * in_bytes + DV * in_bytes + rec) +
             T * DV * out_bytes + 16)
+
+
+def mamba2_decode_bytes_per_token(state_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+    """Algorithmic bytes of one Mamba2 decode step of one sequence (all heads): state read +
+    write, B and C (per group), x, dt, output, slot index."""
+    return (2 * M2_H * M2_N * M2_P * state_bytes + 2 * M2_G * M2_N * in_bytes + M2_H * M2_P * in_bytes +
+            M2_H * in_bytes + M2_H * M2_P * out_bytes + 4)
+
+
+def mamba2_replay_unit_bytes(count: int, fold: bool, ckpt_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
+    """Algorithmic bytes of one Mamba2 ReplaySSM step of one (sequence, head): checkpoint read,
+    `count` buffered entries (raw B + the fp32 record {alpha, delta, 1, 0, w}), the token's
+    inputs (B, C shared by H/G heads), the appended entry (raw B, raw x, record), the output,
+    pointers, and on a fold the checkpoint write."""
+    rec = (4 + M2_P) * 4
+    state = M2_N * M2_P * ckpt_bytes
+    inputs = 2 * M2_N * in_bytes * M2_G // M2_H + M2_P * in_bytes + in_bytes
+    return (state * (2 if fold else 1) + count * (M2_N * in_bytes + rec) + inputs +
+            (M2_N * in_bytes + M2_P * in_bytes + rec) + M2_P * out_bytes + 16)
 
 
 def spec_bytes_per_seq(T: int, state_bytes: int, in_bytes: int = 2, out_bytes: int = 4) -> int:
@@ -365,7 +387,9 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "tokens_per_s": world * B * rsteps / (el / 1e3), "us_per_step": el / rsteps * 1e3, "hbm_gbs": gbs,
             "frac": gbs / peak, "bytes_per_token": total_bytes / rsteps / B, "L": L_RING,
             "start_offsets": "uniform in [0, 15]",
-            "state_write_bytes_per_token": HV * DK * DV * (cs + rs) / L_RING}
+            "state_write_bytes_per_token": HV * DK * DV * (cs + rs) / L_RING,
+            "speedup_vs_decode": (result["ms_per_step"] * 1e3 if cs == 4 else modes["decode_bf16_state"]["us_per_step"])
+            / (el / rsteps * 1e3)}
         result["gpu_launches"] += rsteps
 
         # verify T=4 + rollback, accepted uniform in {0..3}
@@ -420,10 +444,75 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
             "state_write_bytes_per_window_token": HV * DK * DV * ss}
         result["gpu_launches"] += srounds
         del sp
+    result["gpu_launches"] += mamba2_modes(modes, timed, peak, args, world, dev, gen, err, stream)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during the mode runs")
     result["modes"] = modes
     return result
+
+
+def mamba2_modes(modes, timed, peak, args, world, dev, gen, err, stream) -> int:
+    """Mamba2 layer (B = 256, 8 groups, 128 heads, state 128, head dim 64): decode with an fp32 /
+    bf16 state pool of 2B slots, and the ReplaySSM step (L = 16, start offsets in [0, 15]) with an
+    fp32 / bf16 checkpoint. Returns the number of timed launches."""
+    import numpy as np
+    import torch
+
+    from hybrid_ssm_gated_gb300 import gdn
+    from hybrid_ssm_gated_gb300 import workload as wl
+
+    w = wl.WORKLOADS["mamba2_b256_f32"]
+    A_log, dt_bias, D = (torch.from_numpy(t).to(dev) for t in wl.mamba2_params(w))
+    slots = torch.from_numpy(wl.slots(w)).to(dev)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+    x, dt, Bm, Cm = rnd(B, M2_H, M2_P), rnd(B, M2_H), rnd(B, M2_G, M2_N), rnd(B, M2_G, M2_N)
+    out = torch.empty(B, M2_H, M2_P, device=dev)
+    launches = 0
+    msteps = max(20, args.steps // 10)
+    decode_us = {}
+    for name, sdt, ss in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        pool = (torch.randn(2 * B, M2_H, M2_P, M2_N, generator=gen, device=dev) * 0.1).to(sdt)
+        el, lm = timed(lambda: gdn.mamba2_decode_step(pool, slots, x, dt, Bm, Cm, A_log, dt_bias, D, out, err, stream),
+                       msteps, args.warmup)
+        bt = mamba2_decode_bytes_per_token(ss)
+        gbs = bt * B / (lm / 1e3) / 1e9
+        decode_us[name] = el / msteps * 1e3
+        modes[f"mamba2_decode_{name}_state"] = {
+            "tokens_per_s": world * B * msteps / (el / 1e3), "us_per_step": decode_us[name], "hbm_gbs": gbs,
+            "frac": gbs / peak, "bytes_per_token": bt}
+        launches += msteps
+        del pool
+    offsets = wl.start_offsets(wl.WORKLOADS["mamba2_replay_b256_f32"])
+    slot_np = wl.slots(w)
+    for ckname, cdt, cs in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        cache = gdn.ReplayCache.allocate(2 * B, M2_H, M2_N, M2_P, L_RING, cdt, torch.bfloat16, device=dev)
+        cache.ckpt.normal_(0, 0.1, generator=gen)
+        counts = np.zeros(2 * B, dtype=np.int64)
+        counts[slot_np] = offsets
+        cache.pos.copy_(torch.from_numpy(np.repeat(counts[:, None], M2_H, 1).astype(np.int32)))
+        out1 = torch.empty(B, 1, M2_H, M2_P, device=dev)
+        rstep = lambda: gdn.mamba2_replay_step(cache, slots, x, dt, Bm, Cm, A_log, dt_bias, D, out1, err, stream)
+        for _ in range(L_RING):  # the ring holds real entries before timing
+            rstep()
+        torch.cuda.synchronize()
+        cc = (cache.pos - cache.ckpt_pos)[slots.long(), 0].cpu().numpy().astype(np.int64)
+        rsteps = max(32, (args.steps // 20) // L_RING * L_RING)
+        total = 0
+        for _ in range(rsteps):  # host replay of the ring counts: fold when an append would overflow
+            fold = cc + 1 > L_RING
+            total += M2_H * sum(mamba2_replay_unit_bytes(int(c), bool(f), cs) for c, f in zip(cc, fold))
+            cc = np.where(fold, 0, cc) + 1
+        el, lm = timed(rstep, rsteps, 3)
+        gbs = total / rsteps / (lm / 1e3) / 1e9
+        us = el / rsteps * 1e3
+        modes[f"mamba2_replay_step_{ckname}_ckpt"] = {
+            "tokens_per_s": world * B * rsteps / (el / 1e3), "us_per_step": us, "hbm_gbs": gbs, "frac": gbs / peak,
+            "bytes_per_token": total / rsteps / B, "L": L_RING, "start_offsets": "uniform in [0, 15]",
+            "speedup_vs_decode": decode_us[ckname] / us,
+            "state_write_bytes_per_token": M2_H * M2_N * M2_P * cs / L_RING}
+        launches += rsteps
+        del cache
+    return launches
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -491,6 +580,8 @@ def run_case(args) -> None:
              --read-dtype, an fp32 checkpoint plus a read copy of that dtype.
     verify:  T=4 verify windows + rollbacks on the same cache.
     spec:    T=4 speculative steps with one state copy per window token, pool of 5B slots.
+    mamba2_decode / mamba2_replay: the Mamba2 layer (8 groups, 128 heads, state 128, head dim 64),
+             decode on a pool of 2B slots, or ReplaySSM steps with L=16 and offsets in [0, 15].
     """
     import numpy as np
     import torch
@@ -508,7 +599,24 @@ def run_case(args) -> None:
     dt_bias = torch.rand(HV, generator=g, device=dev) * 2 - 1
     slots = torch.randperm(2 * Bc, generator=g, device=dev)[:Bc].to(torch.int32)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    if args.case == "decode":
+    if args.case.startswith("mamba2"):
+        from hybrid_ssm_gated_gb300 import workload as wl
+
+        A2, dt2, D2 = (torch.from_numpy(t).to(dev) for t in wl.mamba2_params(wl.WORKLOADS["mamba2_b256_f32"]))
+        x, dtt, Bm, Cm = rnd(Bc, M2_H, M2_P), rnd(Bc, M2_H), rnd(Bc, M2_G, M2_N), rnd(Bc, M2_G, M2_N)
+        out = torch.empty(Bc, M2_H, M2_P, device=dev)
+        if args.case == "mamba2_decode":
+            pool = (torch.randn(2 * Bc, M2_H, M2_P, M2_N, generator=g, device=dev) * 0.1).to(sdt)
+            for _ in range(args.steps):
+                gdn.mamba2_decode_step(pool, slots, x, dtt, Bm, Cm, A2, dt2, D2, out, err)
+        else:
+            cache = gdn.ReplayCache.allocate(2 * Bc, M2_H, M2_N, M2_P, L_RING, sdt, torch.bfloat16, device=dev)
+            cache.ckpt.normal_(0, 0.1, generator=g)
+            off = torch.randint(0, L_RING, (2 * Bc, 1), generator=g, device=dev).to(torch.int32)
+            cache.pos.copy_(off.expand(2 * Bc, M2_H))
+            for _ in range(args.steps):
+                gdn.mamba2_replay_step(cache, slots, x, dtt, Bm, Cm, A2, dt2, D2, out, err)
+    elif args.case == "decode":
         pool = (torch.randn(2 * Bc, HV, DV, DK, generator=g, device=dev) * 0.1).to(sdt)
         q, k, v, a, b = rnd(Bc, HK, DK), rnd(Bc, HK, DK), rnd(Bc, HV, DV), rnd(Bc, HV), rnd(Bc, HV)
         out = torch.empty(Bc, HV, DV, device=dev)
@@ -557,7 +665,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "replay", "verify", "spec"],
+    ap.add_argument("--case", choices=["decode", "replay", "verify", "spec", "mamba2_decode", "mamba2_replay"],
                     help="run --steps untimed launches of one kernel for a profiler and exit")
     ap.add_argument("--B", type=int, default=B, help="batch of --case")
     ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16", "f16"], help="state dtype of --case")
