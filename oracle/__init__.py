@@ -45,6 +45,8 @@ def lib() -> C.CDLL:
             "orc_replay_rollback": (I, [P, I, I]),
             "orc_replay2_window": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I, P, P, P, P, P, D, D, P]),
             "orc_replay2_flush": (I, [I, I, I, P, I, P, I, P, P, I, P, P, P, I]),
+            "orc_prefill_head": (None, [I, I, I, P, I, P, P, P, I, P, P, I, P]),
+            "orc_prefill": (I, [I, I, I, I, I, I64, P, I, P, P, P, P, P, P, P, I, P, P, I, P, I]),
             "orc_m2_gating": (None, [D, D, D, P, P]),
             "orc_m2_decode_head": (None, [I, I, P, I, P, P, P, I, D, D, D, P]),
             "orc_m2_decode_step": (I, [I, I, I, I, I, I64, P, I, P, P, P, P, P, I, P, P, P, P, I]),
@@ -180,6 +182,46 @@ def spec_step(pool: np.ndarray, sdt, src_slots, dst_slots, q, k, v, a, b, idt, A
     bad = lib().orc_spec_step(B, T, Hk, Hv, dk, dv, num_slots, _ptr(pool), _code(sdt), _ptr(src_slots),
                               _ptr(dst_slots), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(idt),
                               _ptr(A_log), _ptr(dt_bias), _ptr(out), int(nthreads))
+    return out, bad
+
+
+# ---------------------------------------------------------------- prefill
+
+
+def prefill_head(S: np.ndarray, sdt, q, k, v, idt, alpha, beta, interval: int) -> np.ndarray:
+    """Prefill of one head: T tokens from S ([dv, dk] storage array, updated in place), the state
+    rounded to sdt after every `interval` tokens and after the last. Returns out [T, dv] fp64."""
+    assert S.dtype == NPTYPE[_code(sdt)] and S.flags["C_CONTIGUOUS"]
+    dv, dk = S.shape
+    q, k, v = _arr(q, idt), _arr(k, idt), _arr(v, idt)
+    T = q.shape[0]
+    alpha = np.ascontiguousarray(alpha, dtype=np.float64)
+    beta = np.ascontiguousarray(beta, dtype=np.float64)
+    out = np.empty((T, dv), dtype=np.float64)
+    lib().orc_prefill_head(dk, dv, T, _ptr(S), _code(sdt), _ptr(q), _ptr(k), _ptr(v), _code(idt), _ptr(alpha),
+                           _ptr(beta), int(interval), _ptr(out))
+    return out
+
+
+def prefill(pool: np.ndarray, sdt, slots, cu_seqlens, q, k, v, a, b, idt, A_log, dt_bias, interval: int,
+            nthreads: int = 1) -> tuple[np.ndarray, int]:
+    """Prefill of variable-length sequences: sequence i owns tokens cu_seqlens[i]:cu_seqlens[i+1] of
+    q, k [total, Hk, dk], v [total, Hv, dv], a, b [total, Hv]; pool [num_slots, Hv, dv, dk] updated
+    in place. Returns (out [total, Hv, dv] fp64, number of refused units)."""
+    assert pool.dtype == NPTYPE[_code(sdt)] and pool.flags["C_CONTIGUOUS"]
+    num_slots, Hv, dv, dk = pool.shape
+    q, k, v, a, b = (_arr(x, idt) for x in (q, k, v, a, b))
+    slots = np.ascontiguousarray(slots, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    B = slots.shape[0]
+    total = int(cu[-1])
+    Hk = q.size // max(1, total * dk) if total else 1
+    A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+    dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+    out = np.empty((total, Hv, dv), dtype=np.float64)
+    bad = lib().orc_prefill(B, Hk, Hv, dk, dv, num_slots, _ptr(pool), _code(sdt), _ptr(slots), _ptr(cu), _ptr(q),
+                            _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(idt), _ptr(A_log), _ptr(dt_bias), int(interval),
+                            _ptr(out), int(nthreads))
     return out, bad
 
 

@@ -328,6 +328,85 @@ int orc_spec_step(int B, int T, int Hk, int Hv, int dk, int dv, int64_t num_slot
     return bad;
 }
 
+/* ------------------------------------------------------------------ prefill */
+
+/* The tokens one decode step at a time (vLLM PR #52191 summary, 实现拆解 items
+ * 3-4: the chunked kernel keeps the state in an FP32 buffer within a chunk and
+ * writes it back, rounded to the state dtype, at the end of every chunk). */
+void orc_prefill_head(int dk, int dv, int T, void* S, int sdt, const void* q, const void* k, const void* v, int idt,
+                      const double* alpha, const double* beta, int interval, double* out) {
+    int64_t n = (int64_t)dk * dv;
+    double* Sd = (double*)malloc(sizeof(double) * (size_t)n);
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * dk + dv));
+    double *kr = buf, *qr = buf + dk, *kn = buf + 2 * dk, *qn = buf + 3 * dk, *vv = buf + 4 * dk;
+    load_vec(S, 0, (int)n, sdt, Sd);
+    for (int t = 0; t < T; ++t) {
+        load_vec(k, (int64_t)t * dk, dk, idt, kr);
+        load_vec(q, (int64_t)t * dk, dk, idt, qr);
+        load_vec(v, (int64_t)t * dv, dv, idt, vv);
+        orc_l2norm(dk, kr, 1.0, kn);
+        orc_l2norm(dk, qr, 1.0 / sqrt((double)dk), qn);
+        rule_step(dk, dv, Sd, kn, vv, alpha[t], beta[t]);
+        readout(dk, dv, Sd, qn, out + (int64_t)t * dv);
+        if ((t + 1) % interval == 0 || t == T - 1) { /* chunk write-back: round, continue from the stored state */
+            for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);
+            load_vec(S, 0, (int)n, sdt, Sd);
+        }
+    }
+    free(buf);
+    free(Sd);
+}
+
+int orc_prefill(int B, int Hk, int Hv, int dk, int dv, int64_t num_slots, void* pool, int sdt,
+                const int32_t* slots, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,
+                const void* a, const void* b, int idt, const float* A_log, const float* dt_bias, int interval,
+                double* out, int nthreads) {
+    int bad = 0;
+    int group = Hv / Hk;
+    int64_t units = (int64_t)B * Hv;
+    (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad) num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h / group;
+        int t0 = cu_seqlens[bi], T = cu_seqlens[bi + 1] - t0;
+        int32_t slot = slots[bi];
+        if (slot < 0 || slot >= num_slots) {
+            if (slot >= num_slots) bad += 1;
+            for (int t = 0; t < T; ++t)
+                for (int j = 0; j < dv; ++j) out[((int64_t)(t0 + t) * Hv + h) * dv + j] = 0.0;
+            continue;
+        }
+        if (T <= 0) continue;
+        double* al = (double*)malloc(sizeof(double) * (size_t)(2 * T));
+        double* be = al + T;
+        double* o = (double*)malloc(sizeof(double) * (size_t)T * dv);
+        char* qs = (char*)malloc((size_t)T * dk * orc_dtype_size(idt));
+        char* ks = (char*)malloc((size_t)T * dk * orc_dtype_size(idt));
+        char* vs = (char*)malloc((size_t)T * dv * orc_dtype_size(idt));
+        int isz = orc_dtype_size(idt);
+        for (int t = 0; t < T; ++t) { /* gather this head's rows of the sequence */
+            int64_t tok = t0 + t;
+            memcpy(qs + (size_t)t * dk * isz, elem_ptr(q, (tok * Hk + kh) * dk, idt), (size_t)dk * isz);
+            memcpy(ks + (size_t)t * dk * isz, elem_ptr(k, (tok * Hk + kh) * dk, idt), (size_t)dk * isz);
+            memcpy(vs + (size_t)t * dv * isz, elem_ptr(v, (tok * Hv + h) * dv, idt), (size_t)dv * isz);
+            orc_gating(A_log[h], dt_bias[h], orc_load(a, tok * Hv + h, idt), orc_load(b, tok * Hv + h, idt), &al[t],
+                       &be[t]);
+        }
+        void* S = (char*)pool + ((int64_t)slot * Hv + h) * (int64_t)dv * dk * orc_dtype_size(sdt);
+        orc_prefill_head(dk, dv, T, S, sdt, qs, ks, vs, idt, al, be, interval, o);
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < dv; ++j) out[((int64_t)(t0 + t) * Hv + h) * dv + j] = o[(int64_t)t * dv + j];
+        free(vs);
+        free(ks);
+        free(qs);
+        free(o);
+        free(al);
+    }
+    return bad;
+}
+
 /* ------------------------------------------------------------------ ReplaySSM */
 
 /* The fp64 state after the first n buffered entries, rebuilt from S0 by

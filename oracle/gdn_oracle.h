@@ -99,6 +99,25 @@ int orc_replay2_window(int dk, int dv, int L, void* M, int mdt, void* Rd, int rd
 int orc_replay2_flush(int dk, int dv, int L, void* M, int mdt, void* Rd, int rdt, const void* ek, const void* ev,
                       int idt, const double* ealpha, const double* ebeta, int32_t* meta, int force);
 
+/* Prefill of one (sequence, value head): T tokens in order from the state S
+ * (dv*dk elements of sdt), each a plain decode step in fp64. The state is
+ * rounded to sdt after every `interval` tokens (a chunk write-back: the next
+ * chunk starts from the rounded state) and after the last token, which is the
+ * state left in S. out[t*dv + j] = o_t from the unrounded S_t. q, k [T][dk],
+ * v [T][dv] in idt; gates alpha, beta [T]. interval >= 1. */
+void orc_prefill_head(int dk, int dv, int T, void* S, int sdt, const void* q, const void* k, const void* v, int idt,
+                      const double* alpha, const double* beta, int interval, double* out);
+
+/* Prefill of a batch of variable-length sequences: sequence b owns tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 of q, k [total][Hk][dk], v [total][Hv][dv],
+ * a, b [total][Hv]; out [total][Hv][dv]. Its state is pool[slots[b]]; slot < 0
+ * is padding and slot >= num_slots is refused (outputs zero, nothing written).
+ * Returns the number of refused (sequence, head) units. */
+int orc_prefill(int B, int Hk, int Hv, int dk, int dv, int64_t num_slots, void* pool, int sdt,
+                const int32_t* slots, const int32_t* cu_seqlens, const void* q, const void* k, const void* v,
+                const void* a, const void* b, int idt, const float* A_log, const float* dt_bias, int interval,
+                double* out, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
