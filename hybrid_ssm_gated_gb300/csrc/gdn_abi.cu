@@ -231,6 +231,38 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
     return launched(e, fn);
 }
 
+int gdn_prefill(const gdn_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* slots,
+                const int32_t* cu_seqlens, int32_t total_tokens, const void* q, const void* k, const void* v,
+                const void* a, const void* b, int32_t in_dtype, const float* A_log, const float* dt_bias,
+                int32_t state_write_interval, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {
+    const char* fn = "gdn_prefill";
+    int rc = check_dims(dims, fn);
+    if (rc) return rc;
+    if (state_write_interval < 1) return fail(GDN_ERR_WINDOW, "%s: state_write_interval=%d < 1", fn, state_write_interval);
+    if (total_tokens < 0) return fail(GDN_ERR_SHAPE, "%s: total_tokens=%d < 0", fn, total_tokens);
+    if ((int64_t)total_tokens * dims->Hv > (int64_t)INT32_MAX / 8)
+        return fail(GDN_ERR_SHAPE, "%s: total_tokens*Hv too large", fn);
+    if (dims->B == 0) return GDN_OK;
+    if (!state_pool || !slots || !cu_seqlens || !dev_err)
+        return fail(GDN_ERR_NULL, "%s: state_pool, slots, cu_seqlens or dev_err is NULL", fn);
+    if (!dtype_ok(state_dtype)) return fail(GDN_ERR_DTYPE, "%s: unsupported state dtype %d", fn, state_dtype);
+    rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
+    if (rc) return rc;
+    if (!aligned16(state_pool) || !aligned_to(slots, 4) || !aligned_to(cu_seqlens, 4) || !aligned_to(dev_err, 4))
+        return fail(GDN_ERR_ALIGN, "%s: state_pool must be 16-byte aligned", fn);
+    gdn::PrefillArgs p{};
+    p.pool = state_pool, p.slots = slots, p.cu_seqlens = cu_seqlens;
+    p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias;
+    p.out = out, p.dev_err = dev_err;
+    p.num_slots = dims->num_slots;
+    p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.total = total_tokens;
+    p.interval = state_write_interval;
+    p.in_dtype = in_dtype, p.out_dtype = out_dtype;
+    p.row_blocks = (dims->dv + gdn::PF_ROWS - 1) / gdn::PF_ROWS;
+    p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
+    return launched(gdn::dispatch_prefill(state_dtype, dims->dk, p, static_cast<cudaStream_t>(stream)), fn);
+}
+
 int gdn_replay_step(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots, const void* q,
                     const void* k, const void* v, const void* a, const void* b, int32_t in_dtype, const float* A_log,
                     const float* dt_bias, void* out, int32_t out_dtype, int32_t* dev_err, void* stream) {

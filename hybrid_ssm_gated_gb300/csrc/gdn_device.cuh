@@ -93,6 +93,18 @@ __device__ __forceinline__ bool wait_tag(const volatile int* tag, int want) {
     return true;
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), tracked
+// by commit groups; cp_async_wait<N> returns once at most N groups of this
+// thread are still in flight (the copies always complete: no flag is polled).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // L2 policy for data read once (state tiles): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

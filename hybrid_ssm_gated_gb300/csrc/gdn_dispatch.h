@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_decode.cuh"
+#include "gdn_prefill.cuh"
 #include "gdn_replay.cuh"
 #include "gdn_spec.cuh"
 
@@ -32,6 +33,9 @@ cudaError_t dispatch_mamba2_replay_f16(int dk, int tmax, ReplayArgs& a, cudaStre
 cudaError_t dispatch_spec_f32(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_spec_bf16(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
 cudaError_t dispatch_spec_f16(int dk, int tmax, SpecArgs& a, cudaStream_t stream, bool& too_big);
+
+// Prefill with a rounded write-back per chunk.
+cudaError_t dispatch_prefill(int state_dtype, int dk, PrefillArgs& a, cudaStream_t stream);
 
 cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
                             int B, int Hv, int T, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);

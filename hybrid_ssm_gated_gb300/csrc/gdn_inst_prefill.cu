@@ -1,0 +1,40 @@
+// Instantiations of the prefill kernel (state dtype x dk) and its launch.
+#include "gdn_dispatch.h"
+#include "gdn_launch.cuh"
+#include "gdn_prefill.cuh"
+
+namespace gdn {
+
+template <typename ST, int DK>
+cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
+    auto kern = prefill_kernel<ST, DK>;
+    const int isz = dtype_size(a.in_dtype);
+    a.raw_bytes = PF_TC * (2 * DK + PF_ROWS) * isz;
+    a.off_kqn = 2 * a.raw_bytes;
+    a.off_qk = a.off_kqn + PF_TC * 2 * DK * 4;
+    a.off_gates = a.off_qk + PF_TC * 4;
+    const int smem = a.off_gates + 2 * PF_TC * 8;
+    int bps = 0;
+    cudaError_t e = prepare_kernel(kern, PF_WARPS * 32, smem, bps);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)a.B * a.Hv * a.row_blocks;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, PF_WARPS * 32, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch_prefill(int state_dtype, int dk, PrefillArgs& a, cudaStream_t s) {
+#define GDN_PF(CODE, ST)                                    \
+    if (state_dtype == CODE) {                              \
+        if (dk == 32) return launch_prefill<ST, 32>(a, s);  \
+        if (dk == 64) return launch_prefill<ST, 64>(a, s);  \
+        if (dk == 128) return launch_prefill<ST, 128>(a, s); \
+    }
+    GDN_PF(GDN_F32, float)
+    GDN_PF(GDN_BF16, __nv_bfloat16)
+    GDN_PF(GDN_F16, __half)
+#undef GDN_PF
+    return cudaErrorNotSupported;
+}
+
+}  // namespace gdn

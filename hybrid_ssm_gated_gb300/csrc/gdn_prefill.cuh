@@ -1,0 +1,273 @@
+// gdn_prefill.cuh -- prefill of the gated delta rule with a rounded state
+// write-back per chunk (gdn_prefill).
+//
+// Semantics (vLLM PR #52191 summary, section 实现拆解 items 3-4: the chunked
+// kernel works on an FP32 copy of the state within a chunk and writes it back,
+// rounded to the state dtype, at the end of each chunk): the tokens of a
+// sequence run through the rule in order; the state is rounded to its storage
+// dtype after every `interval` tokens and after the last one, and only the
+// final state is stored. Outputs come from the unrounded FP32 state.
+//
+// Kernel shape. One CTA per (sequence, value head, block of 64 state rows);
+// each of its 4 warps keeps 16 rows of S in FP32 registers for the whole
+// sequence, so the state is read once and written once. Tokens are staged in
+// chunks of PF_TC through shared memory with 16-byte asynchronous copies,
+// double buffered: while a chunk is processed the next one is in flight.
+// Per chunk, the warps first normalise its keys and queries (one token per
+// warp at a time) into an FP32 table, so the row loop only reads them; then
+// every warp runs the chunk's tokens over its rows -- two dot products, the
+// rank-one update and the output per row, reduced over the LPR lanes that
+// hold a row. Rows are independent given the token, so warps never wait for
+// one another inside a chunk. The step is bound by FP32 arithmetic
+// (7 dk dv flops per token and head), not by memory.
+#pragma once
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+
+struct PrefillArgs {
+    void* pool;
+    const int32_t* slots;
+    const int32_t* cu_seqlens;  // [B + 1] token offsets
+    const void* q;              // [total][Hk][dk]
+    const void* k;
+    const void* v;  // [total][Hv][dv]
+    const void* a;  // [total][Hv]
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+    void* out;  // [total][Hv][dv]
+    int32_t* dev_err;
+    int64_t num_slots;
+    int B, Hk, Hv, dv, total, interval;
+    int in_dtype, out_dtype;
+    int row_blocks;  // ceil(dv / PF_ROWS)
+    float q_scale;
+    // dynamic shared memory layout, bytes
+    int raw_bytes;  // one staged chunk: q, k [TC][dk] and v [TC][PF_ROWS] in the input dtype
+    int off_kqn, off_qk, off_gates;
+};
+
+constexpr int PF_WARPS = 4;
+constexpr int PF_ROWS = 64;  // state rows per CTA, 16 per warp
+constexpr int PF_TC = 16;    // tokens per staged chunk
+#ifndef GDN_PREFILL_MIN_BLOCKS
+#define GDN_PREFILL_MIN_BLOCKS 4  // CTAs per SM the register budget must allow
+#endif
+
+template <typename ST, int DK>
+struct PrefillCfg {
+    static constexpr int VEC = Store<ST>::VEC;  // state elements per 16 bytes
+    static constexpr int E = 16;                // state elements per lane per row
+    static constexpr int NC = E / VEC;
+    static constexpr int LPR = DK / E;       // lanes per row
+    static constexpr int RPP = 32 / LPR;     // rows per warp pass
+    static constexpr int PASSES = 16 / RPP;  // passes covering a warp's 16 rows
+    static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
+    static_assert(DK % E == 0 && 16 % RPP == 0, "unsupported dk");
+};
+
+template <typename ST, int DK>
+__global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill_kernel(const PrefillArgs p) {
+    using C = PrefillCfg<ST, DK>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = blockIdx.x % p.row_blocks;
+    const int unit = blockIdx.x / p.row_blocks;
+    const int bseq = unit / p.Hv, h = unit - bseq * p.Hv, kh = h / (p.Hv / p.Hk);
+    const int slot = p.slots[bseq];
+    const int t0 = p.cu_seqlens[bseq], t1 = p.cu_seqlens[bseq + 1];
+    if (t0 < 0 || t1 < t0 || t1 > p.total) {
+        if (threadIdx.x == 0 && rb == 0 && h == 0) set_error(p.dev_err, GDN_DEVERR_SEQLEN);
+        return;
+    }
+    const int T = t1 - t0;
+    const int row0 = rb * PF_ROWS;
+    const int nrows = min(PF_ROWS, p.dv - row0);  // a multiple of 16
+    if (slot < 0 || slot >= p.num_slots) {
+        if (slot >= p.num_slots && threadIdx.x == 0 && rb == 0) set_error(p.dev_err, GDN_DEVERR_SLOT);
+        for (int i = threadIdx.x; i < T * nrows; i += blockDim.x) {
+            const int t = i / nrows, r = i - t * nrows;
+            store_elem(p.out, ((int64_t)(t0 + t) * p.Hv + h) * p.dv + row0 + r, p.out_dtype, 0.f);
+        }
+        return;
+    }
+    if (T == 0) return;
+
+    const int isz = dtype_size(p.in_dtype);
+    auto raw = [&](int c) { return smem + (c & 1) * p.raw_bytes; };  // staged chunk c
+    float* kqn = reinterpret_cast<float*>(smem + p.off_kqn);     // [TC][2][DK] normalised k, q
+    float* qkb = reinterpret_cast<float*>(smem + p.off_qk);      // [TC] q.k
+    float2* gts = reinterpret_cast<float2*>(smem + p.off_gates);  // [2][TC] (alpha, beta)
+    const int qbytes = DK * isz, vbytes = nrows * isz;
+    const int nchunks = (T + PF_TC - 1) / PF_TC;
+
+    // stage chunk c (its q, k rows and this block's slice of v) into buffer c & 1
+    auto stage = [&](int c) {
+        unsigned char* dst = raw(c);
+        const int n = min(PF_TC, T - c * PF_TC);
+        const int per_tok = 2 * (qbytes / 16) + vbytes / 16;  // 16-byte pieces per token
+        for (int i = threadIdx.x; i < n * per_tok; i += blockDim.x) {
+            const int t = i / per_tok, x = i - t * per_tok;
+            const int64_t tok = t0 + c * PF_TC + t;
+            const char* src;
+            unsigned char* d;
+            if (x < 2 * (qbytes / 16)) {
+                const int which = x / (qbytes / 16), piece = x - which * (qbytes / 16);
+                src = static_cast<const char*>(which ? p.k : p.q) + (tok * p.Hk + kh) * qbytes + piece * 16;
+                d = dst + (which * PF_TC + t) * qbytes + piece * 16;
+            } else {
+                const int piece = x - 2 * (qbytes / 16);
+                src = static_cast<const char*>(p.v) + ((tok * p.Hv + h) * p.dv + row0) * isz + piece * 16;
+                d = dst + 2 * PF_TC * qbytes + t * PF_ROWS * isz + piece * 16;
+            }
+            cp_async16(d, src);
+        }
+        cp_async_commit();
+    };
+    // gates of chunk c, one thread per token
+    auto gate = [&](int c, float& al, float& be) {
+        const int t = c * PF_TC + threadIdx.x;
+        al = 0.f, be = 0.f;
+        if (threadIdx.x < PF_TC && t < T) {
+            const int64_t gi = (int64_t)(t0 + t) * p.Hv + h;
+            gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype), load_elem(p.b, gi, p.in_dtype), al, be);
+        }
+    };
+
+    // this lane's rows and element positions
+    const int pg = lane % C::LPR, rsub = lane / C::LPR;
+    const int wrow = warp * 16;               // the warp's first row within the block
+    const bool wvalid = wrow < nrows;         // whole warps are valid or not (nrows % 16 == 0)
+    auto pos_of = [&](int cc) { return (cc * C::LPR + pg) * C::VEC; };
+    unsigned char* gstate =
+        static_cast<unsigned char*>(p.pool) + (((int64_t)slot * p.Hv + h) * p.dv + row0) * C::ROW_BYTES;
+
+    stage(0);
+    {
+        float al, be;
+        gate(0, al, be);
+        if (threadIdx.x < PF_TC) gts[threadIdx.x] = make_float2(al, be);
+    }
+    float S[C::PASSES][C::E];
+    if (wvalid) {
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            const int r = wrow + ps * C::RPP + rsub;
+#pragma unroll
+            for (int cc = 0; cc < C::NC; ++cc)
+                load_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
+        }
+    }
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int n = min(PF_TC, T - c * PF_TC);
+        float nal = 0.f, nbe = 0.f;
+        if (c + 1 < nchunks) {
+            stage(c + 1);
+            gate(c + 1, nal, nbe);
+            cp_async_wait<1>();  // chunk c has landed (this thread's copies)
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // every thread's copies of chunk c are visible
+
+        // normalised keys and queries of the chunk, one token per warp at a time
+        const unsigned char* src = raw(c);
+        for (int t = warp; t < n; t += PF_WARPS) {
+            float kx[DK / 32], qx[DK / 32];
+            float ssk = 0.f, ssq = 0.f;
+#pragma unroll
+            for (int e = 0; e < DK / 32; ++e) {
+                kx[e] = load_elem(src + (PF_TC + t) * qbytes, lane + 32 * e, p.in_dtype);
+                qx[e] = load_elem(src + t * qbytes, lane + 32 * e, p.in_dtype);
+                ssk = fmaf(kx[e], kx[e], ssk), ssq = fmaf(qx[e], qx[e], ssq);
+            }
+            const float ik = rsqrtf(group_sum<32>(ssk) + 1e-6f);
+            const float iq = rsqrtf(group_sum<32>(ssq) + 1e-6f) * p.q_scale;
+            float kq = 0.f;
+#pragma unroll
+            for (int e = 0; e < DK / 32; ++e) {
+                kx[e] *= ik, qx[e] *= iq;
+                kq = fmaf(kx[e], qx[e], kq);
+                kqn[(t * 2) * DK + lane + 32 * e] = kx[e];
+                kqn[(t * 2 + 1) * DK + lane + 32 * e] = qx[e];
+            }
+            kq = group_sum<32>(kq);
+            if (lane == 0) qkb[t] = kq;
+        }
+        __syncthreads();  // the table is complete
+
+        if (wvalid) {
+            const float2* g = gts + (c & 1) * PF_TC;
+            for (int t = 0; t < n; ++t) {
+                float2 k2[C::E / 2], q2[C::E / 2];
+#pragma unroll
+                for (int cc = 0; cc < C::NC; ++cc) {
+#pragma unroll
+                    for (int e = 0; e < C::VEC; e += 4) {
+                        const float4 kv = *reinterpret_cast<const float4*>(kqn + (t * 2) * DK + pos_of(cc) + e);
+                        const float4 qv = *reinterpret_cast<const float4*>(kqn + (t * 2 + 1) * DK + pos_of(cc) + e);
+                        const int i = (cc * C::VEC + e) / 2;
+                        k2[i] = make_float2(kv.x, kv.y), k2[i + 1] = make_float2(kv.z, kv.w);
+                        q2[i] = make_float2(qv.x, qv.y), q2[i + 1] = make_float2(qv.z, qv.w);
+                    }
+                }
+                const float2 gab = g[t];
+                const float al = gab.x, be = gab.y, qk = qkb[t];
+                const float2 al2 = make_float2(al, al);
+                const unsigned char* vrow = src + 2 * PF_TC * qbytes + t * PF_ROWS * isz;
+                const int64_t obase = ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0;
+#pragma unroll
+                for (int ps = 0; ps < C::PASSES; ++ps) {
+                    float2 u2 = make_float2(0.f, 0.f), p2 = u2;
+#pragma unroll
+                    for (int e = 0; e < C::E / 2; ++e) {
+                        const float2 s2 = make_float2(S[ps][2 * e], S[ps][2 * e + 1]);
+                        u2 = __ffma2_rn(s2, k2[e], u2);
+                        p2 = __ffma2_rn(s2, q2[e], p2);
+                    }
+                    const float u = group_sum<C::LPR>(u2.x + u2.y);
+                    const float pq = group_sum<C::LPR>(p2.x + p2.y);
+                    const int r = wrow + ps * C::RPP + rsub;
+                    const float vj = load_elem(vrow, r, p.in_dtype);
+                    const float delta = be * (vj - al * u);
+                    const float2 d2 = make_float2(delta, delta);
+#pragma unroll
+                    for (int e = 0; e < C::E / 2; ++e) {
+                        const float2 r2 = __ffma2_rn(k2[e], d2, __fmul2_rn(make_float2(S[ps][2 * e], S[ps][2 * e + 1]), al2));
+                        S[ps][2 * e] = r2.x, S[ps][2 * e + 1] = r2.y;
+                    }
+                    if (pg == 0) store_elem(p.out, obase + r, p.out_dtype, fmaf(al, pq, qk * delta));
+                }
+                // chunk write-back: the state continues as stored (rounded), except after the last token,
+                // which is stored below
+                const int s = c * PF_TC + t + 1;  // tokens done
+                if constexpr (!std::is_same<ST, float>::value) {
+                    if (s % p.interval == 0 && s < T) {
+#pragma unroll
+                        for (int ps = 0; ps < C::PASSES; ++ps)
+#pragma unroll
+                            for (int cc = 0; cc < C::NC; ++cc)
+                                Store<ST>::unpack(Store<ST>::pack(S[ps] + cc * C::VEC), S[ps] + cc * C::VEC);
+                    }
+                }
+            }
+        }
+        if (c + 1 < nchunks && threadIdx.x < PF_TC) gts[((c + 1) & 1) * PF_TC + threadIdx.x] = make_float2(nal, nbe);
+        __syncthreads();  // buffer c & 1 and the table are free again
+    }
+
+    if (wvalid) {
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            const int r = wrow + ps * C::RPP + rsub;
+#pragma unroll
+            for (int cc = 0; cc < C::NC; ++cc)
+                store_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
+        }
+    }
+}
+
+}  // namespace gdn

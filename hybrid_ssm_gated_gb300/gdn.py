@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gdn.h")
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
-DEVERR_SLOT, DEVERR_RING, DEVERR_ACCEPT, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_SLOT, DEVERR_RING, DEVERR_ACCEPT, DEVERR_TIMEOUT, DEVERR_SEQLEN = 1, 2, 4, 8, 16
 
 
 class GdnError(RuntimeError):
@@ -51,6 +51,7 @@ _P = C.c_void_p
 _I = C.c_int32
 _SIGS = {
     "gdn_decode_step": [C.POINTER(gdn_dims), _P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P],
+    "gdn_prefill": [C.POINTER(gdn_dims), _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I, _P, _I, _P, _P],
     "gdn_spec_step": [C.POINTER(gdn_dims), _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P],
     "gdn_replay_step": [C.POINTER(gdn_dims), C.POINTER(gdn_replay_cache), _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                         _I, _P, _P],
@@ -155,6 +156,20 @@ def gdn_spec_step(state_pool, src_slots, dst_slots, q, k, v, a, b, A_log, dt_bia
     _check(lib().gdn_spec_step(C.byref(d), _ptr(state_pool), _code(state_pool), _ptr(src_slots), _ptr(dst_slots),
                                int(T), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(q), _ptr(A_log),
                                _ptr(dt_bias), _ptr(out), _code(out), _ptr(dev_err), _stream(stream)))
+
+
+def gdn_prefill(state_pool, slots, cu_seqlens, q, k, v, a, b, A_log, dt_bias, out, dev_err, state_write_interval: int,
+                stream=None) -> None:
+    """Prefill of variable-length sequences: state_pool [num_slots, Hv, dv, dk]; slots [B] int32;
+    cu_seqlens [B + 1] int32 (device); q, k [total, Hk, dk]; v [total, Hv, dv]; a, b [total, Hv];
+    out [total, Hv, dv]; the state rounded to its dtype every state_write_interval tokens."""
+    num_slots, Hv, dv, dk = state_pool.shape
+    total = q.shape[0]
+    d = make_dims(slots.shape[0], q.shape[-2], Hv, dk, dv, num_slots)
+    _check(lib().gdn_prefill(C.byref(d), _ptr(state_pool), _code(state_pool), _ptr(slots), _ptr(cu_seqlens),
+                             int(total), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _code(q), _ptr(A_log),
+                             _ptr(dt_bias), int(state_write_interval), _ptr(out), _code(out), _ptr(dev_err),
+                             _stream(stream)))
 
 
 class ReplayCache:

@@ -31,7 +31,8 @@ DTYPE_CODE = {"f32": F32, "bf16": BF16, "f16": F16}
 DTYPE_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
 
 # Seed-stream tags: each kind of draw has its own stream.
-_TAG_PARAMS, _TAG_STATE, _TAG_STEP, _TAG_SLOTS, _TAG_OFFSETS, _TAG_ACCEPT, _TAG_M2_PARAMS, _TAG_M2_STEP = range(8)
+(_TAG_PARAMS, _TAG_STATE, _TAG_STEP, _TAG_SLOTS, _TAG_OFFSETS, _TAG_ACCEPT, _TAG_M2_PARAMS, _TAG_M2_STEP,
+ _TAG_PREFILL) = range(9)
 
 
 @dataclass(frozen=True)
@@ -59,6 +60,7 @@ class Workload:
     L: int = 0
     T: int = 1
     max_offset: int = 0
+    prefill_len: int = 0  # tokens per sequence of a prefill workload
 
     def __post_init__(self):
         if self.num_slots == 0:
@@ -91,6 +93,8 @@ WORKLOADS = {
                                 L=16, T=4),
     "verify_b256_bf16": Workload("verify_b256_bf16", B=256, Hk=16, Hv=32, dk=128, dv=128, steps=32,
                                  state_dtype="bf16", L=16, T=4),
+    # Prefill of 19 sequences of 2048 tokens, state written back every 64 tokens.
+    "prefill_b19_f32": Workload("prefill_b19_f32", B=19, Hk=16, Hv=32, dk=128, dv=128, steps=1, prefill_len=2048),
     # Mamba2 layer of 128 heads, head dim 64, state dim 128, 8 groups (Hk = G, Hv = H, dk = N, dv = P).
     "mamba2_b256_f32": Workload("mamba2_b256_f32", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64),
     "mamba2_b256_bf16": Workload("mamba2_b256_bf16", B=256, Hk=8, Hv=128, dk=128, dv=64, steps=64,
@@ -227,5 +231,19 @@ def mamba2_step_inputs(w: Workload, step: int) -> dict[str, np.ndarray]:
     out = {}
     for name, shape in (("x", (w.B, T, w.Hv, w.dv)), ("dt", (w.B, T, w.Hv)), ("Bm", (w.B, T, w.Hk, w.dk)),
                         ("Cm", (w.B, T, w.Hk, w.dk))):
+        out[name] = quantize(r.standard_normal(shape, dtype=np.float32), w.in_dtype)
+    return out
+
+
+# ---------------------------------------------------------------- prefill draws
+
+
+def prefill_inputs(w: Workload, total: int, call: int = 0) -> dict[str, np.ndarray]:
+    """Activations of `total` prefill tokens: q, k [total, Hk, dk]; v [total, Hv, dv]; a, b [total, Hv];
+    ~ N(0,1) in the input dtype."""
+    r = _rng(w, _TAG_PREFILL, call)
+    out = {}
+    for name, shape in (("q", (total, w.Hk, w.dk)), ("k", (total, w.Hk, w.dk)), ("v", (total, w.Hv, w.dv)),
+                        ("a", (total, w.Hv)), ("b", (total, w.Hv))):
         out[name] = quantize(r.standard_normal(shape, dtype=np.float32), w.in_dtype)
     return out

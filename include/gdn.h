@@ -76,6 +76,7 @@ extern "C" {
 #define GDN_DEVERR_RING 2    /* replay count pos - ckpt_pos outside [0, L], or a rollback below ckpt_pos */
 #define GDN_DEVERR_ACCEPT 4  /* accepted count outside [0, T-1] */
 #define GDN_DEVERR_TIMEOUT 8 /* an internal pipeline wait gave up (should never happen) */
+#define GDN_DEVERR_SEQLEN 16 /* prefill token offsets decreasing or beyond total_tokens */
 
 /* Element types of states, activations and outputs; mirrors the fp32 /
  * bf16 / fp16 choice of a mamba SSM cache dtype. */
@@ -236,6 +237,30 @@ int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const 
  */
 int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
                  const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream);
+
+/*
+ * gdn_prefill -- prefill of variable-length sequences with the state written
+ * back once per chunk (vLLM PR #52191 summary, section 实现拆解 items 3-4:
+ * the chunked kernel updates an FP32 copy of the state and writes it back,
+ * rounded to the state dtype, at the end of every chunk).
+ * Sequence b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 and the state
+ * pool[slots[b]]; its tokens run through the rule in order, the state being
+ * rounded to state_dtype after every state_write_interval tokens (the next
+ * chunk continues from the rounded state) and after the last token, which is
+ * what is stored. Outputs come from the unrounded FP32 state.
+ * cu_seqlens   [B + 1] int32 device array, 0 <= cu_seqlens[b] <= cu_seqlens[b+1]
+ *              <= total_tokens (otherwise GDN_DEVERR_SEQLEN and the sequence
+ *              is skipped).
+ * q, k         [total_tokens][Hk][dk];  v [total_tokens][Hv][dv];
+ * a, b         [total_tokens][Hv];      out [total_tokens][Hv][dv].
+ * state_write_interval >= 1 (GDN_ERR_WINDOW otherwise). A padding slot zeroes
+ * its sequence's outputs; an out-of-range slot also sets GDN_DEVERR_SLOT. An
+ * empty sequence leaves its state untouched.
+ */
+int gdn_prefill(const gdn_dims* dims, void* state_pool, int32_t state_dtype, const int32_t* slots,
+                const int32_t* cu_seqlens, int32_t total_tokens, const void* q, const void* k, const void* v,
+                const void* a, const void* b, int32_t in_dtype, const float* A_log, const float* dt_bias,
+                int32_t state_write_interval, void* out, int32_t out_dtype, int32_t* dev_err, void* stream);
 
 /*
  * ---------------------------------------------------------------- Mamba2

@@ -197,3 +197,23 @@ def test_mamba2_rejections(lib):
     assert lib.mamba2_replay_flush(C.byref(_m2dims(N=48)), C.byref(_cache()), FAKE, 1, FAKE, None) == -3
     assert lib.mamba2_rollback(C.byref(d), C.byref(_cache(L=4)), FAKE, FAKE, 5, FAKE, None) == -4
     assert lib.mamba2_rollback(C.byref(_m2dims(B=0)), C.byref(_cache()), None, None, 4, None, None) == 0
+
+
+def _prefill(lib, dims, interval=64, total=32, pool=FAKE, cu=FAKE, q=FAKE, b=FAKE, idt=1, err=FAKE):
+    return lib.gdn_prefill(C.byref(dims), pool, 0, FAKE, cu, total, q, FAKE, FAKE, FAKE, b, idt, FAKE, FAKE, interval,
+                           FAKE, 0, err, None)
+
+
+def test_prefill_rejections(lib):
+    d = _dims()
+    assert _prefill(lib, d, interval=0) == -4  # GDN_ERR_WINDOW
+    assert _prefill(lib, d, total=-1) == -3
+    assert _prefill(lib, _dims(dk=96)) == -3
+    assert _prefill(lib, d, cu=None) == -1
+    assert _prefill(lib, d, b=None) == -1
+    assert _prefill(lib, d, err=None) == -1
+    assert _prefill(lib, d, idt=9) == -2
+    assert _prefill(lib, d, q=FAKE + 4) == -5
+    assert _prefill(lib, d, pool=FAKE + 8) == -5
+    assert _prefill(lib, d, total=1 << 30) == -3  # total_tokens * Hv too large
+    assert _prefill(lib, _dims(B=0), pool=None, cu=None) == 0
