@@ -445,10 +445,64 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         result["gpu_launches"] += srounds
         del sp
     result["gpu_launches"] += mamba2_modes(modes, timed, peak, args, world, dev, gen, err, stream)
+    result["gpu_launches"] += prefill_modes(modes, timed, args, world, dev, gen, err, stream)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during the mode runs")
     result["modes"] = modes
     return result
+
+
+def fp32_alu_peak_tflops(dev) -> tuple[float, str]:
+    """FP32 FMA peak: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock."""
+    import torch
+
+    props = torch.cuda.get_device_properties(dev)
+    mhz = None
+    try:
+        q = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                           capture_output=True, text=True, timeout=10)
+        mhz = float(q.stdout.strip().splitlines()[0])
+    except Exception:
+        pass
+    if not mhz:
+        mhz = 2070.0
+    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, f"{props.multi_processor_count} SMs x 128 x 2 x {mhz:.0f} MHz"
+
+
+def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
+    """Prefill of 19 sequences of 2048 tokens (Hk=16, Hv=32, dk=dv=128, bf16 activations), state written
+    back every 64 tokens, fp32 and bf16 state: tokens/s and the FP32 rate of the rule's 7 dk dv flops per
+    token and head against the FP32 FMA peak. Returns the number of timed launches."""
+    import numpy as np
+    import torch
+
+    from hybrid_ssm_gated_gb300 import gdn
+    from hybrid_ssm_gated_gb300 import workload as wl
+
+    w = wl.WORKLOADS["prefill_b19_f32"]
+    total = w.B * w.prefill_len
+    cu = torch.from_numpy(np.arange(w.B + 1, dtype=np.int32) * w.prefill_len).to(dev)
+    slots = torch.from_numpy(wl.slots(w)).to(dev)
+    A_log, dt_bias = (torch.from_numpy(t).to(dev) for t in wl.head_params(w))
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+    q, k, v = rnd(total, w.Hk, w.dk), rnd(total, w.Hk, w.dk), rnd(total, w.Hv, w.dv)
+    a, b = rnd(total, w.Hv), rnd(total, w.Hv)
+    out = torch.empty(total, w.Hv, w.dv, device=dev)
+    peak, peak_note = fp32_alu_peak_tflops(dev)
+    flops = 7 * w.dk * w.dv * w.Hv * total
+    calls = max(5, args.steps // 200)
+    for name, sdt in (("fp32", torch.float32), ("bf16", torch.bfloat16)):
+        pool = (torch.randn(w.num_slots, w.Hv, w.dv, w.dk, generator=gen, device=dev) * 0.1).to(sdt)
+        el, lm = timed(lambda: gdn.gdn_prefill(pool, slots, cu, q, k, v, a, b, A_log, dt_bias, out, err, 64, stream),
+                       calls, 3)
+        tf = flops / (lm / 1e3) / 1e12
+        modes[f"prefill_{name}_state"] = {
+            "tokens_per_s": world * total * calls / (el / 1e3), "us_per_call": el / calls * 1e3,
+            "sequences": w.B, "tokens_per_sequence": w.prefill_len, "state_write_interval": 64,
+            "bound": "alu", "alu_tflops": tf, "alu_peak_tflops": peak, "frac": tf / peak, "peak_derivation": peak_note,
+            "flops_per_token": flops / total}
+        del pool
+    return 2 * calls
 
 
 def mamba2_modes(modes, timed, peak, args, world, dev, gen, err, stream) -> int:
@@ -582,6 +636,7 @@ def run_case(args) -> None:
     spec:    T=4 speculative steps with one state copy per window token, pool of 5B slots.
     mamba2_decode / mamba2_replay: the Mamba2 layer (8 groups, 128 heads, state 128, head dim 64),
              decode on a pool of 2B slots, or ReplaySSM steps with L=16 and offsets in [0, 15].
+    prefill: B sequences of 2048 tokens, state written back every 64 tokens.
     """
     import numpy as np
     import torch
@@ -599,7 +654,16 @@ def run_case(args) -> None:
     dt_bias = torch.rand(HV, generator=g, device=dev) * 2 - 1
     slots = torch.randperm(2 * Bc, generator=g, device=dev)[:Bc].to(torch.int32)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    if args.case.startswith("mamba2"):
+    if args.case == "prefill":
+        Tp = 2048
+        cu = torch.arange(Bc + 1, device=dev, dtype=torch.int32) * Tp
+        q, k, v = rnd(Bc * Tp, HK, DK), rnd(Bc * Tp, HK, DK), rnd(Bc * Tp, HV, DV)
+        a, b = rnd(Bc * Tp, HV), rnd(Bc * Tp, HV)
+        pool = (torch.randn(2 * Bc, HV, DV, DK, generator=g, device=dev) * 0.1).to(sdt)
+        out = torch.empty(Bc * Tp, HV, DV, device=dev)
+        for _ in range(args.steps):
+            gdn.gdn_prefill(pool, slots, cu, q, k, v, a, b, A_log, dt_bias, out, err, 64)
+    elif args.case.startswith("mamba2"):
         from hybrid_ssm_gated_gb300 import workload as wl
 
         A2, dt2, D2 = (torch.from_numpy(t).to(dev) for t in wl.mamba2_params(wl.WORKLOADS["mamba2_b256_f32"]))
@@ -665,7 +729,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "replay", "verify", "spec", "mamba2_decode", "mamba2_replay"],
+    ap.add_argument("--case", choices=["decode", "replay", "verify", "spec", "mamba2_decode", "mamba2_replay",
+                                       "prefill"],
                     help="run --steps untimed launches of one kernel for a profiler and exit")
     ap.add_argument("--B", type=int, default=B, help="batch of --case")
     ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16", "f16"], help="state dtype of --case")

@@ -148,6 +148,23 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
+// Reduce-scatter of x[0..N) over aligned groups of N lanes: afterwards lane
+// (group position g) holds the group total of x[g].
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&x)[N], int g) {
+#pragma unroll
+    for (int half = N / 2; half >= 1; half >>= 1) {
+        const bool upper = (g & half) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? x[i] : x[i + half];
+            const float keep = upper ? x[i + half] : x[i];
+            x[i] = keep + __shfl_xor_sync(FULL_MASK, send, half);
+        }
+    }
+    return x[0];
+}
+
 // ------------------------------------------------------------------ elements
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }

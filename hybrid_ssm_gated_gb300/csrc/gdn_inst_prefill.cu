@@ -12,7 +12,9 @@ cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
     a.raw_bytes = PF_TC * (2 * DK + PF_ROWS) * isz;
     a.off_kqn = 2 * a.raw_bytes;
     a.off_qk = a.off_kqn + PF_TC * 2 * DK * 4;
-    a.off_gates = a.off_qk + PF_TC * 4;
+    a.off_vf = a.off_qk + align_up(PF_TC * 4, 16);
+    a.off_of = a.off_vf + PF_TC * PF_ROWS * 4;
+    a.off_gates = a.off_of + PF_TC * PF_ROWS * 4;
     const int smem = a.off_gates + 2 * PF_TC * 8;
     int bps = 0;
     cudaError_t e = prepare_kernel(kern, PF_WARPS * 32, smem, bps);

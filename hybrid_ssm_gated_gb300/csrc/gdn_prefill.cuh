@@ -13,13 +13,23 @@
 // sequence, so the state is read once and written once. Tokens are staged in
 // chunks of PF_TC through shared memory with 16-byte asynchronous copies,
 // double buffered: while a chunk is processed the next one is in flight.
-// Per chunk, the warps first normalise its keys and queries (one token per
-// warp at a time) into an FP32 table, so the row loop only reads them; then
-// every warp runs the chunk's tokens over its rows -- two dot products, the
-// rank-one update and the output per row, reduced over the LPR lanes that
-// hold a row. Rows are independent given the token, so warps never wait for
-// one another inside a chunk. The step is bound by FP32 arithmetic
-// (7 dk dv flops per token and head), not by memory.
+// Per chunk, the warps first normalise its keys and queries and convert its
+// values (one token per warp at a time) into FP32 tables, so the row loop only
+// reads them; then every warp runs the chunk's tokens over its rows: two dot
+// products per row, whose 2 x PASSES partial sums over the LPR lanes of a row
+// group are finished by one reduce-scatter (lane g of the group then owns one
+// sum), the correction and output of one row per lane pair, the corrections
+// broadcast back, and the rank-one update. Outputs go to a shared-memory tile
+// and leave, coalesced and in the output dtype, once per chunk. Rows are
+// independent given the token, so warps never wait for one another inside a
+// chunk. The step is bound by FP32 arithmetic (7 dk dv flops per token and
+// head), not by memory.
+// The decay is applied lazily: the registers hold S / sigma, sigma being the
+// product of the decays since the last rescale (uniform over the CTA), so a
+// token's update is one fused multiply-add per element, S/sigma' += k
+// (delta / sigma'), instead of a multiply and an add. The registers are
+// rescaled when sigma falls below 2^-32 (or a decay underflows), at every
+// write-back (where the rounding happens on sigma S) and at the end.
 #pragma once
 
 #include "gdn_device.cuh"
@@ -46,12 +56,15 @@ struct PrefillArgs {
     float q_scale;
     // dynamic shared memory layout, bytes
     int raw_bytes;  // one staged chunk: q, k [TC][dk] and v [TC][PF_ROWS] in the input dtype
-    int off_kqn, off_qk, off_gates;
+    int off_kqn, off_qk, off_vf, off_of, off_gates;
 };
 
 constexpr int PF_WARPS = 4;
 constexpr int PF_ROWS = 64;  // state rows per CTA, 16 per warp
-constexpr int PF_TC = 16;    // tokens per staged chunk
+#ifndef GDN_PREFILL_TOKENS
+#define GDN_PREFILL_TOKENS 16
+#endif
+constexpr int PF_TC = GDN_PREFILL_TOKENS;  // tokens per staged chunk
 #ifndef GDN_PREFILL_MIN_BLOCKS
 #define GDN_PREFILL_MIN_BLOCKS 4  // CTAs per SM the register budget must allow
 #endif
@@ -65,7 +78,7 @@ struct PrefillCfg {
     static constexpr int RPP = 32 / LPR;     // rows per warp pass
     static constexpr int PASSES = 16 / RPP;  // passes covering a warp's 16 rows
     static constexpr int ROW_BYTES = DK * (int)sizeof(ST);
-    static_assert(DK % E == 0 && 16 % RPP == 0, "unsupported dk");
+    static_assert(DK % E == 0 && 16 % RPP == 0 && 2 * PASSES == LPR, "unsupported dk");
 };
 
 template <typename ST, int DK>
@@ -99,6 +112,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
     auto raw = [&](int c) { return smem + (c & 1) * p.raw_bytes; };  // staged chunk c
     float* kqn = reinterpret_cast<float*>(smem + p.off_kqn);     // [TC][2][DK] normalised k, q
     float* qkb = reinterpret_cast<float*>(smem + p.off_qk);      // [TC] q.k
+    float* vf = reinterpret_cast<float*>(smem + p.off_vf);       // [TC][PF_ROWS] v in FP32
+    float* of = reinterpret_cast<float*>(smem + p.off_of);       // [TC][PF_ROWS] outputs
     float2* gts = reinterpret_cast<float2*>(smem + p.off_gates);  // [2][TC] (alpha, beta)
     const int qbytes = DK * isz, vbytes = nrows * isz;
     const int nchunks = (T + PF_TC - 1) / PF_TC;
@@ -150,7 +165,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         gate(0, al, be);
         if (threadIdx.x < PF_TC) gts[threadIdx.x] = make_float2(al, be);
     }
-    float S[C::PASSES][C::E];
+    float S[C::PASSES][C::E];  // the state divided by sig
+    float sig = 1.f;
+    int until_wb = p.interval;  // tokens until the next write-back
     if (wvalid) {
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps) {
@@ -196,6 +213,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             }
             kq = group_sum<32>(kq);
             if (lane == 0) qkb[t] = kq;
+            for (int r = lane; r < nrows; r += 32)
+                vf[t * PF_ROWS + r] = load_elem(src + 2 * PF_TC * qbytes + t * PF_ROWS * isz, r, p.in_dtype);
         }
         __syncthreads();  // the table is complete
 
@@ -216,9 +235,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                 }
                 const float2 gab = g[t];
                 const float al = gab.x, be = gab.y, qk = qkb[t];
-                const float2 al2 = make_float2(al, al);
-                const unsigned char* vrow = src + 2 * PF_TC * qbytes + t * PF_ROWS * isz;
-                const int64_t obase = ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0;
+                // partial sums: x[2 ps] = S[:, row of pass ps] . k, x[2 ps + 1] = . q
+                float x[2 * C::PASSES];
 #pragma unroll
                 for (int ps = 0; ps < C::PASSES; ++ps) {
                     float2 u2 = make_float2(0.f, 0.f), p2 = u2;
@@ -228,35 +246,64 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                         u2 = __ffma2_rn(s2, k2[e], u2);
                         p2 = __ffma2_rn(s2, q2[e], p2);
                     }
-                    const float u = group_sum<C::LPR>(u2.x + u2.y);
-                    const float pq = group_sum<C::LPR>(p2.x + p2.y);
-                    const int r = wrow + ps * C::RPP + rsub;
-                    const float vj = load_elem(vrow, r, p.in_dtype);
-                    const float delta = be * (vj - al * u);
+                    x[2 * ps] = u2.x + u2.y, x[2 * ps + 1] = p2.x + p2.y;
+                }
+                // lane pg of the row group now owns sum pg: (pass pg / 2, k or q); a lane pair
+                // finishes the row of its pass
+                const float mine = reduce_scatter<2 * C::PASSES>(x, pg);
+                const float other = __shfl_xor_sync(FULL_MASK, mine, 1);
+                const float u = sig * ((pg & 1) ? other : mine), pq = sig * ((pg & 1) ? mine : other);
+                const int rme = wrow + (pg >> 1) * C::RPP + rsub;
+                const float delta_me = be * (vf[t * PF_ROWS + rme] - al * u);
+                if ((pg & 1) == 0) of[t * PF_ROWS + rme] = fmaf(al, pq, qk * delta_me);
+                // S_t = alpha S_{t-1} + k delta^T with S_{t-1} = sig S: the registers keep S_t / (sig alpha)
+                float sn = sig * al;
+                if (sn < 0x1p-32f) {  // uniform over the CTA: fold the decay into the registers
+#pragma unroll
+                    for (int ps = 0; ps < C::PASSES; ++ps)
+#pragma unroll
+                        for (int e = 0; e < C::E; ++e) S[ps][e] *= sn;
+                    sn = 1.f;
+                }
+                const float inv = __frcp_rn(sn);
+#pragma unroll
+                for (int ps = 0; ps < C::PASSES; ++ps) {
+                    const float delta = __shfl_sync(FULL_MASK, delta_me, 2 * ps, C::LPR) * inv;
                     const float2 d2 = make_float2(delta, delta);
 #pragma unroll
                     for (int e = 0; e < C::E / 2; ++e) {
-                        const float2 r2 = __ffma2_rn(k2[e], d2, __fmul2_rn(make_float2(S[ps][2 * e], S[ps][2 * e + 1]), al2));
+                        const float2 r2 = __ffma2_rn(k2[e], d2, make_float2(S[ps][2 * e], S[ps][2 * e + 1]));
                         S[ps][2 * e] = r2.x, S[ps][2 * e + 1] = r2.y;
                     }
-                    if (pg == 0) store_elem(p.out, obase + r, p.out_dtype, fmaf(al, pq, qk * delta));
                 }
-                // chunk write-back: the state continues as stored (rounded), except after the last token,
-                // which is stored below
-                const int s = c * PF_TC + t + 1;  // tokens done
-                if constexpr (!std::is_same<ST, float>::value) {
-                    if (s % p.interval == 0 && s < T) {
+                sig = sn;
+                // chunk write-back: the state continues as stored (sig S rounded), except after the last
+                // token, which is stored below
+                if (--until_wb == 0) {
+                    until_wb = p.interval;
+                    if (c * PF_TC + t + 1 < T) {  // the registers become the stored state exactly
 #pragma unroll
                         for (int ps = 0; ps < C::PASSES; ++ps)
 #pragma unroll
-                            for (int cc = 0; cc < C::NC; ++cc)
-                                Store<ST>::unpack(Store<ST>::pack(S[ps] + cc * C::VEC), S[ps] + cc * C::VEC);
+                            for (int cc = 0; cc < C::NC; ++cc) {
+                                float* x = S[ps] + cc * C::VEC;
+#pragma unroll
+                                for (int e = 0; e < C::VEC; ++e) x[e] *= sig;
+                                if constexpr (!std::is_same<ST, float>::value) Store<ST>::unpack(Store<ST>::pack(x), x);
+                            }
+                        sig = 1.f;
                     }
                 }
             }
         }
         if (c + 1 < nchunks && threadIdx.x < PF_TC) gts[((c + 1) & 1) * PF_TC + threadIdx.x] = make_float2(nal, nbe);
-        __syncthreads();  // buffer c & 1 and the table are free again
+        __syncthreads();  // buffer c & 1 and the tables are free again; the output tile is complete
+        // the chunk's outputs, coalesced along the rows of each token
+        for (int i = threadIdx.x; i < n * nrows; i += blockDim.x) {
+            const int t = i / nrows, r = i - t * nrows;
+            store_elem(p.out, ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0 + r, p.out_dtype,
+                       of[t * PF_ROWS + r]);
+        }
     }
 
     if (wvalid) {
@@ -264,8 +311,11 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         for (int ps = 0; ps < C::PASSES; ++ps) {
             const int r = wrow + ps * C::RPP + rsub;
 #pragma unroll
-            for (int cc = 0; cc < C::NC; ++cc)
+            for (int cc = 0; cc < C::NC; ++cc) {
+#pragma unroll
+                for (int e = 0; e < C::VEC; ++e) S[ps][cc * C::VEC + e] *= sig;
                 store_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
+            }
         }
     }
 }

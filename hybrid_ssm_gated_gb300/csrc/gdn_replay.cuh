@@ -165,23 +165,6 @@ struct ReplayMeta {
 };
 static_assert(sizeof(ReplayMeta) <= REPLAY_META, "meta too large");
 
-// Reduce-scatter of x[0..N) over aligned groups of N lanes: afterwards lane
-// (group position g) holds the group total of x[g].
-template <int N>
-__device__ __forceinline__ float reduce_scatter(float (&x)[N], int g) {
-#pragma unroll
-    for (int half = N / 2; half >= 1; half >>= 1) {
-        const bool upper = (g & half) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? x[i] : x[i + half];
-            const float keep = upper ? x[i + half] : x[i];
-            x[i] = keep + __shfl_xor_sync(FULL_MASK, send, half);
-        }
-    }
-    return x[0];
-}
-
 // Reduce-scatter of V values over aligned groups of G lanes (powers of two):
 // halving steps while a lane holds more than one value, then butterfly
 // steps. Afterwards lane g holds group totals in x[0..max(1, V/G)): values

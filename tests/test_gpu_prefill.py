@@ -31,11 +31,11 @@ def _cu(lens):
     return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
 
 
-def _gpu_prefill(pool_gpu, slots, cu, x, w, interval, out_dtype="f32"):
+def _gpu_prefill(pool_gpu, slots, cu, x, w, interval, out_dtype="f32", params=None):
     xd = step_to_device(x, w.in_dtype)
     total = int(cu[-1])
     out = torch.full((total, w.Hv, w.dv), 7.0, dtype=TORCH_DT[out_dtype], device="cuda")
-    A_log, dt_bias = wl.head_params(w)
+    A_log, dt_bias = wl.head_params(w) if params is None else params
     err = dev_err()
     gdn.gdn_prefill(pool_gpu, torch.from_numpy(np.asarray(slots, np.int32)).cuda(), torch.from_numpy(cu).cuda(),
                     xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], torch.from_numpy(A_log).cuda(),
@@ -44,14 +44,14 @@ def _gpu_prefill(pool_gpu, slots, cu, x, w, interval, out_dtype="f32"):
     return out, int(err.item())
 
 
-def _check_all(w, lens, slots, interval, out_dtype="f32", expect_err=0):
+def _check_all(w, lens, slots, interval, out_dtype="f32", expect_err=0, params=None):
     cu = _cu(lens)
     pool = wl.initial_pool(w)
     pool_gpu = dev(pool, w.state_dtype)
     x = wl.prefill_inputs(w, int(cu[-1]))
-    out, err = _gpu_prefill(pool_gpu, slots, cu, x, w, interval, out_dtype)
+    out, err = _gpu_prefill(pool_gpu, slots, cu, x, w, interval, out_dtype, params)
     assert err == expect_err
-    A_log, dt_bias = wl.head_params(w)
+    A_log, dt_bias = wl.head_params(w) if params is None else params
     ref, bad = oracle.prefill(pool, w.state_dtype, slots, cu, x["q"], x["k"], x["v"], x["a"], x["b"], w.in_dtype,
                               A_log, dt_bias, interval, nthreads=8)
     got = to_f64(out)
@@ -81,6 +81,14 @@ def test_prefill_small_all_elements(sdt, idt, interval):
 def test_prefill_other_head_shapes(dk, dv, Hk, Hv, sdt):
     w = wl.Workload("pfh", B=4, Hk=Hk, Hv=Hv, dk=dk, dv=dv, steps=1, state_dtype=sdt, in_dtype="bf16", seed=62)
     _check_all(w, [3, 16, 40, 0], wl.slots(w), 8)
+
+
+@pytest.mark.parametrize("sdt", ["f32", "bf16"])
+def test_prefill_extreme_decays(sdt):
+    # decays near 1, tiny ones and ones that underflow FP32 (A_log = 5, dt_bias = 5: alpha ~ e^-740)
+    w = wl.Workload("pfx", B=3, Hk=1, Hv=4, dk=64, dv=64, steps=1, state_dtype=sdt, in_dtype="f32", seed=66)
+    params = (np.array([-4.0, 1.0, 3.0, 5.0], np.float32), np.array([-6.0, 0.0, 2.0, 5.0], np.float32))
+    _check_all(w, [40, 70, 17], wl.slots(w), 16, params=params)
 
 
 def test_prefill_padding_out_of_range_and_narrow_output():
