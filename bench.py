@@ -311,7 +311,8 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         "bytes_per_token": bpt,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps in groups of 4, 6 chunk stages)", "launch_us": launch_ms * 1e3,
+                     "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps in groups of 4, 6 chunk stages)",
+                     "launch_us": launch_ms * 1e3,
                      "algorithmic_bytes_per_launch": bpt * B},
         "clocks": clocks,
         "gpu_launches": args.steps,
@@ -459,14 +460,15 @@ def fp32_alu_peak_tflops(dev) -> tuple[float, str]:
     props = torch.cuda.get_device_properties(dev)
     mhz = None
     try:
-        q = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
-                           capture_output=True, text=True, timeout=10)
+        q = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=clocks.max.sm",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
         mhz = float(q.stdout.strip().splitlines()[0])
     except Exception:
         pass
     if not mhz:
         mhz = 2070.0
-    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, f"{props.multi_processor_count} SMs x 128 x 2 x {mhz:.0f} MHz"
+    sms = props.multi_processor_count
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"{sms} SMs x 128 x 2 x {mhz:.0f} MHz"
 
 
 def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
