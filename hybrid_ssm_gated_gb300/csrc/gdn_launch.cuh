@@ -84,8 +84,9 @@ cudaError_t prepare_kernel(Kernel kern, int threads, int smem, int& blocks_per_s
 #ifndef GDN_DECODE_CHUNK_STAGES_NARROW
 #define GDN_DECODE_CHUNK_STAGES_NARROW 8
 #endif
+// head stages: units in flight per CTA (6 measured best for 16-bit states: 4 left them short of data)
 #ifndef GDN_DECODE_HEAD_STAGES
-#define GDN_DECODE_HEAD_STAGES 4
+#define GDN_DECODE_HEAD_STAGES 6
 #endif
 constexpr int DEC_NCW = GDN_DECODE_CONSUMER_WARPS, DEC_NH = GDN_DECODE_HEAD_STAGES;
 template <typename ST>
