@@ -248,8 +248,9 @@ int gdn_prefill(const gdn_dims* dims, void* state_pool, int32_t state_dtype, con
     if (!dtype_ok(state_dtype)) return fail(GDN_ERR_DTYPE, "%s: unsupported state dtype %d", fn, state_dtype);
     rc = check_activations(fn, q, k, v, a, b, in_dtype, A_log, dt_bias, out, out_dtype);
     if (rc) return rc;
-    if (!aligned16(state_pool) || !aligned_to(slots, 4) || !aligned_to(cu_seqlens, 4) || !aligned_to(dev_err, 4))
-        return fail(GDN_ERR_ALIGN, "%s: state_pool must be 16-byte aligned", fn);
+    if (!aligned16(state_pool) || !aligned16(out) || !aligned_to(slots, 4) || !aligned_to(cu_seqlens, 4) ||
+        !aligned_to(dev_err, 4))
+        return fail(GDN_ERR_ALIGN, "%s: state_pool and out must be 16-byte aligned", fn);
     gdn::PrefillArgs p{};
     p.pool = state_pool, p.slots = slots, p.cu_seqlens = cu_seqlens;
     p.q = q, p.k = k, p.v = v, p.a = a, p.b = b, p.A_log = A_log, p.dt_bias = dt_bias;

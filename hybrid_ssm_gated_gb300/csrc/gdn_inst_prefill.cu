@@ -15,7 +15,7 @@ cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
     a.off_vf = a.off_qk + align_up(PF_TC * 4, 16);
     a.off_of = a.off_vf + PF_TC * PF_ROWS * 4;
     a.off_gates = a.off_of + PF_TC * PF_ROWS * 4;
-    const int smem = a.off_gates + 2 * PF_TC * 8;
+    const int smem = a.off_gates + 2 * PF_TC * 16;
     int bps = 0;
     cudaError_t e = prepare_kernel(kern, PF_WARPS * 32, smem, bps);
     if (e != cudaSuccess) return e;

@@ -19,7 +19,10 @@
 // products per row, whose 2 x PASSES partial sums over the LPR lanes of a row
 // group are finished by one reduce-scatter (lane g of the group then owns one
 // sum), the correction and output of one row per lane pair, the corrections
-// broadcast back, and the rank-one update. Outputs go to a shared-memory tile
+// broadcast back, and the rank-one update. A lane keeps the row of pass
+// p ^ (g >> 1) in its register slot p: partners in the reduce-scatter's pass
+// levels then hold each other's values in the same slots, so those levels
+// need no per-lane selects. Outputs go to a shared-memory tile
 // and leave, coalesced and in the output dtype, once per chunk. Rows are
 // independent given the token, so warps never wait for one another inside a
 // chunk. The step is bound by FP32 arithmetic (7 dk dv flops per token and
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
     float* qkb = reinterpret_cast<float*>(smem + p.off_qk);      // [TC] q.k
     float* vf = reinterpret_cast<float*>(smem + p.off_vf);       // [TC][PF_ROWS] v in FP32
     float* of = reinterpret_cast<float*>(smem + p.off_of);       // [TC][PF_ROWS] outputs
-    float2* gts = reinterpret_cast<float2*>(smem + p.off_gates);  // [2][TC] (alpha, beta)
+    float4* gts = reinterpret_cast<float4*>(smem + p.off_gates);  // [2][TC] (alpha, beta, 1 / alpha, 0)
     const int qbytes = DK * isz, vbytes = nrows * isz;
     const int nchunks = (T + PF_TC - 1) / PF_TC;
 
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         cp_async_commit();
     };
     // gates of chunk c, one thread per token
-    auto gate = [&](int c, float& al, float& be) {
+    auto gate = [&](int c, float& al, float& be) {  // and 1 / alpha, below
         const int t = c * PF_TC + threadIdx.x;
         al = 0.f, be = 0.f;
         if (threadIdx.x < PF_TC && t < T) {
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
 
     // this lane's rows and element positions
     const int pg = lane % C::LPR, rsub = lane / C::LPR;
+    const int pq_bits = pg >> 1;  // register slot s holds the row of pass s ^ pq_bits
     const int wrow = warp * 16;               // the warp's first row within the block
     const bool wvalid = wrow < nrows;         // whole warps are valid or not (nrows % 16 == 0)
     auto pos_of = [&](int cc) { return (cc * C::LPR + pg) * C::VEC; };
@@ -163,15 +167,15 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
     {
         float al, be;
         gate(0, al, be);
-        if (threadIdx.x < PF_TC) gts[threadIdx.x] = make_float2(al, be);
+        if (threadIdx.x < PF_TC) gts[threadIdx.x] = make_float4(al, be, 1.f / al, 0.f);
     }
     float S[C::PASSES][C::E];  // the state divided by sig
-    float sig = 1.f;
+    float sig = 1.f, isig = 1.f;  // sig and 1 / sig (a product of the decays' reciprocals, re-taken per chunk)
     int until_wb = p.interval;  // tokens until the next write-back
     if (wvalid) {
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps) {
-            const int r = wrow + ps * C::RPP + rsub;
+            const int r = wrow + (ps ^ pq_bits) * C::RPP + rsub;
 #pragma unroll
             for (int cc = 0; cc < C::NC; ++cc)
                 load_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
@@ -219,7 +223,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         __syncthreads();  // the table is complete
 
         if (wvalid) {
-            const float2* g = gts + (c & 1) * PF_TC;
+            const float4* g = gts + (c & 1) * PF_TC;
+            isig = __frcp_rn(sig);  // re-taken once per chunk, so the products drift by at most 16 roundings
             for (int t = 0; t < n; ++t) {
                 float2 k2[C::E / 2], q2[C::E / 2];
 #pragma unroll
@@ -233,9 +238,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                         q2[i] = make_float2(qv.x, qv.y), q2[i + 1] = make_float2(qv.z, qv.w);
                     }
                 }
-                const float2 gab = g[t];
-                const float al = gab.x, be = gab.y, qk = qkb[t];
-                // partial sums: x[2 ps] = S[:, row of pass ps] . k, x[2 ps + 1] = . q
+                const float4 gab = g[t];
+                const float al = gab.x, be = gab.y, ial = gab.z, qk = qkb[t];
+                // partial sums: x[2 s] = S[:, row in slot s] . k, x[2 s + 1] = . q
                 float x[2 * C::PASSES];
 #pragma unroll
                 for (int ps = 0; ps < C::PASSES; ++ps) {
@@ -248,27 +253,37 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                     }
                     x[2 * ps] = u2.x + u2.y, x[2 * ps + 1] = p2.x + p2.y;
                 }
-                // lane pg of the row group now owns sum pg: (pass pg / 2, k or q); a lane pair
-                // finishes the row of its pass
-                const float mine = reduce_scatter<2 * C::PASSES>(x, pg);
+                // Reduce-scatter over the row group. Slot s of lane g holds pass s ^ (g >> 1), so across a
+                // pass level (lane bit h >= 2) partner g ^ h keeps in slot i + h what this lane keeps in
+                // slot i: every lane sends its upper half and adds into its lower half. The last level
+                // (the k/q bit) is the usual one. Lane pg then owns (pass pg / 2, k or q); a lane pair
+                // finishes the row of its pass.
+                float mine;
+                {
+#pragma unroll
+                    for (int half = C::PASSES; half >= 2; half >>= 1)
+#pragma unroll
+                        for (int i = 0; i < half; ++i) x[i] += __shfl_xor_sync(FULL_MASK, x[i + half], half);
+                    const bool odd = (pg & 1) != 0;
+                    mine = (odd ? x[1] : x[0]) + __shfl_xor_sync(FULL_MASK, odd ? x[0] : x[1], 1);
+                }
                 const float other = __shfl_xor_sync(FULL_MASK, mine, 1);
                 const float u = sig * ((pg & 1) ? other : mine), pq = sig * ((pg & 1) ? mine : other);
                 const int rme = wrow + (pg >> 1) * C::RPP + rsub;
                 const float delta_me = be * (vf[t * PF_ROWS + rme] - al * u);
                 if ((pg & 1) == 0) of[t * PF_ROWS + rme] = fmaf(al, pq, qk * delta_me);
                 // S_t = alpha S_{t-1} + k delta^T with S_{t-1} = sig S: the registers keep S_t / (sig alpha)
-                float sn = sig * al;
+                float sn = sig * al, inv = isig * ial;
                 if (sn < 0x1p-32f) {  // uniform over the CTA: fold the decay into the registers
 #pragma unroll
                     for (int ps = 0; ps < C::PASSES; ++ps)
 #pragma unroll
                         for (int e = 0; e < C::E; ++e) S[ps][e] *= sn;
-                    sn = 1.f;
+                    sn = 1.f, inv = 1.f;
                 }
-                const float inv = __frcp_rn(sn);
 #pragma unroll
                 for (int ps = 0; ps < C::PASSES; ++ps) {
-                    const float delta = __shfl_sync(FULL_MASK, delta_me, 2 * ps, C::LPR) * inv;
+                    const float delta = __shfl_sync(FULL_MASK, delta_me, 2 * (ps ^ pq_bits), C::LPR) * inv;
                     const float2 d2 = make_float2(delta, delta);
 #pragma unroll
                     for (int e = 0; e < C::E / 2; ++e) {
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                         S[ps][2 * e] = r2.x, S[ps][2 * e + 1] = r2.y;
                     }
                 }
-                sig = sn;
+                sig = sn, isig = inv;
                 // chunk write-back: the state continues as stored (sig S rounded), except after the last
                 // token, which is stored below
                 if (--until_wb == 0) {
@@ -291,25 +306,38 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                                 for (int e = 0; e < C::VEC; ++e) x[e] *= sig;
                                 if constexpr (!std::is_same<ST, float>::value) Store<ST>::unpack(Store<ST>::pack(x), x);
                             }
-                        sig = 1.f;
+                        sig = 1.f, isig = 1.f;
                     }
                 }
             }
         }
-        if (c + 1 < nchunks && threadIdx.x < PF_TC) gts[((c + 1) & 1) * PF_TC + threadIdx.x] = make_float2(nal, nbe);
+        if (c + 1 < nchunks && threadIdx.x < PF_TC)
+            gts[((c + 1) & 1) * PF_TC + threadIdx.x] = make_float4(nal, nbe, 1.f / nal, 0.f);
         __syncthreads();  // buffer c & 1 and the tables are free again; the output tile is complete
-        // the chunk's outputs, coalesced along the rows of each token
-        for (int i = threadIdx.x; i < n * nrows; i += blockDim.x) {
-            const int t = i / nrows, r = i - t * nrows;
-            store_elem(p.out, ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0 + r, p.out_dtype,
-                       of[t * PF_ROWS + r]);
+        // the chunk's outputs, coalesced along the rows of each token, four at a time
+        const int q4 = nrows / 4;
+        for (int i = threadIdx.x; i < n * q4; i += blockDim.x) {
+            const int t = i / q4, r = (i - t * q4) * 4;
+            const float4 o = *reinterpret_cast<const float4*>(of + t * PF_ROWS + r);
+            const int64_t oi = ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0 + r;
+            if (p.out_dtype == GDN_F32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = o;
+            } else {
+                const float ov[4] = {o.x, o.y, o.z, o.w};
+                uint32_t w[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    w[e] = p.out_dtype == GDN_BF16 ? pack_bf16x2(ov[2 * e], ov[2 * e + 1])
+                                                   : pack_f16x2(ov[2 * e], ov[2 * e + 1]);
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(w[0], w[1]);
+            }
         }
     }
 
     if (wvalid) {
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps) {
-            const int r = wrow + ps * C::RPP + rsub;
+            const int r = wrow + (ps ^ pq_bits) * C::RPP + rsub;
 #pragma unroll
             for (int cc = 0; cc < C::NC; ++cc) {
 #pragma unroll

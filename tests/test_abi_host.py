@@ -199,9 +199,9 @@ def test_mamba2_rejections(lib):
     assert lib.mamba2_rollback(C.byref(_m2dims(B=0)), C.byref(_cache()), None, None, 4, None, None) == 0
 
 
-def _prefill(lib, dims, interval=64, total=32, pool=FAKE, cu=FAKE, q=FAKE, b=FAKE, idt=1, err=FAKE):
+def _prefill(lib, dims, interval=64, total=32, pool=FAKE, cu=FAKE, q=FAKE, b=FAKE, idt=1, err=FAKE, out=FAKE):
     return lib.gdn_prefill(C.byref(dims), pool, 0, FAKE, cu, total, q, FAKE, FAKE, FAKE, b, idt, FAKE, FAKE, interval,
-                           FAKE, 0, err, None)
+                           out, 0, err, None)
 
 
 def test_prefill_rejections(lib):
@@ -215,5 +215,6 @@ def test_prefill_rejections(lib):
     assert _prefill(lib, d, idt=9) == -2
     assert _prefill(lib, d, q=FAKE + 4) == -5
     assert _prefill(lib, d, pool=FAKE + 8) == -5
+    assert _prefill(lib, d, out=FAKE + 8) == -5  # outputs leave in 16-byte vectors
     assert _prefill(lib, d, total=1 << 30) == -3  # total_tokens * Hv too large
     assert _prefill(lib, _dims(B=0), pool=None, cu=None) == 0
