@@ -62,11 +62,14 @@ struct DecodeArgs {
 #ifndef GDN_DECODE_UNIT_WARPS
 #define GDN_DECODE_UNIT_WARPS 4
 #endif
+#ifndef GDN_DECODE_UNIT_WARPS_MAMBA2
+#define GDN_DECODE_UNIT_WARPS_MAMBA2 2  // Mamba2 has no per-unit normalisation: smaller groups measured best
+#endif
 
 constexpr int CHUNK_BYTES = 16384;
 constexpr int DV_MAX = 256;
 
-template <typename ST, int DK, int NCW, int NS, int NH>
+template <typename ST, int DK, int NCW, int NS, int NH, int RULE = RULE_GDN>
 struct DecodeCfg {
     static constexpr int VEC = Store<ST>::VEC;  // elements per 16-byte vector
     static constexpr int E = 16;                // state elements per lane per row
@@ -83,7 +86,8 @@ struct DecodeCfg {
     static constexpr int THREADS = (NCW + 1) * 32;
     // warps per unit: a unit's passes are dealt over UW warps, the NG = NCW / UW groups taking
     // units in turn
-    static constexpr int UW = GDN_DECODE_UNIT_WARPS < NCW ? GDN_DECODE_UNIT_WARPS : NCW;
+    static constexpr int UW_ = RULE == RULE_GDN ? GDN_DECODE_UNIT_WARPS : GDN_DECODE_UNIT_WARPS_MAMBA2;
+    static constexpr int UW = UW_ < NCW ? UW_ : NCW;
     static constexpr int NG = NCW / UW;
     static_assert(NCW % UW == 0, "unit warps must divide the consumer warps");
     static_assert(DK % E == 0 && LPR <= 32, "dk must be a multiple of 16 and at most 512");
@@ -91,7 +95,7 @@ struct DecodeCfg {
 
 template <typename ST, int DK, int NCW, int NS, int NH, int RULE = RULE_GDN>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeArgs p) {
-    using C = DecodeCfg<ST, DK, NCW, NS, NH>;
+    using C = DecodeCfg<ST, DK, NCW, NS, NH, RULE>;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* chunks = smem;
     unsigned char* heads = smem + NS * CHUNK_BYTES;

@@ -97,7 +97,7 @@ constexpr int decode_stages() {
 template <typename ST, int DK, int RULE = RULE_GDN>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int NS = decode_stages<ST>();
-    using C = DecodeCfg<ST, DK, DEC_NCW, NS, DEC_NH>;
+    using C = DecodeCfg<ST, DK, DEC_NCW, NS, DEC_NH, RULE>;
     auto kern = decode_kernel<ST, DK, DEC_NCW, NS, DEC_NH, RULE>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
