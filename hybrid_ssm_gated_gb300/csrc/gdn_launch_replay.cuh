@@ -12,7 +12,7 @@ namespace gdn {
 // four warps, so producer + consumers is kept a multiple of four: 16 warps
 // leave 128 registers a thread, 12 leave 168, 8 leave 255.
 #ifndef GDN_REPLAY_WARPS_STEP
-#define GDN_REPLAY_WARPS_STEP 15
+#define GDN_REPLAY_WARPS_STEP 11
 #endif
 #ifndef GDN_REPLAY_WARPS_W4
 #define GDN_REPLAY_WARPS_W4 11
@@ -20,13 +20,9 @@ namespace gdn {
 #ifndef GDN_REPLAY_WARPS_W8
 #define GDN_REPLAY_WARPS_W8 7
 #endif
-#ifndef GDN_REPLAY_WARPS_STEP_MAMBA2
-#define GDN_REPLAY_WARPS_STEP_MAMBA2 11  // Mamba2 units are half as many rows: fewer warps measured best
-#endif
-template <int TMAX, int RULE = RULE_GDN>
+template <int TMAX>
 constexpr int replay_warps() {
-    return TMAX == 1 ? (RULE == RULE_GDN ? GDN_REPLAY_WARPS_STEP : GDN_REPLAY_WARPS_STEP_MAMBA2)
-                     : (TMAX <= 4 ? GDN_REPLAY_WARPS_W4 : GDN_REPLAY_WARPS_W8);
+    return TMAX == 1 ? GDN_REPLAY_WARPS_STEP : (TMAX <= 4 ? GDN_REPLAY_WARPS_W4 : GDN_REPLAY_WARPS_W8);
 }
 
 #ifndef GDN_REPLAY_MAX_HEADS
@@ -73,7 +69,7 @@ int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
 // RULE: the recurrence (gated delta rule or Mamba2).
 template <typename ST, int DK, int TMAX, typename MT = ST, int RULE = RULE_GDN>
 cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
-    constexpr int NCW = replay_warps<TMAX, RULE>();
+    constexpr int NCW = replay_warps<TMAX>();
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
     auto kern = replay_kernel<ST, DK, TMAX, NCW, MT, RULE>;
     DeviceInfo di;
