@@ -1,6 +1,6 @@
 """Compile the CPU oracle (plain C, gcc) into oracle/lib/liboracle.so.
 
-Test infrastructure: building the oracle is part of building the checker,
+Test infrastructure: building the oracle is part of building the tests,
 not of the product path. OpenMP is used when the compiler supports it.
 """
 from __future__ import annotations
