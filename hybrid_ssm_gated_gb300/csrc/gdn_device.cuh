@@ -79,20 +79,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
-// Wait until a shared-memory tag holds `want` (a message published with a
-// fence before the tag store); false after WAIT_LIMIT_NS. Tags carry unit or
-// chunk numbers that are never reused within a launch, so unlike an mbarrier
-// parity wait a slow waiter cannot mistake an older round for its own.
-__device__ __forceinline__ bool wait_tag(const volatile int* tag, int want) {
-    if (*tag == want) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (*tag != want) {
-        __nanosleep(32);
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-    }
-    return true;
-}
-
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), tracked
 // by commit groups; cp_async_wait<N> returns once at most N groups of this
 // thread are still in flight (the copies always complete: no flag is polled).
