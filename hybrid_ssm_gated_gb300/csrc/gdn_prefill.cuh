@@ -8,8 +8,8 @@
 // dtype after every `interval` tokens and after the last one, and only the
 // final state is stored. Outputs come from the unrounded FP32 state.
 //
-// Kernel shape. One CTA per (sequence, value head, block of 64 state rows);
-// each of its 4 warps keeps 16 rows of S in FP32 registers for the whole
+// Kernel shape. One CTA per (sequence, value head, block of 128 state rows);
+// each of its 8 warps keeps 16 rows of S in FP32 registers for the whole
 // sequence, so the state is read once and written once. Tokens are staged in
 // chunks of PF_TC through shared memory with 16-byte asynchronous copies,
 // double buffered: while a chunk is processed the next one is in flight.
@@ -62,14 +62,17 @@ struct PrefillArgs {
     int off_kqn, off_qk, off_vf, off_of, off_gates;
 };
 
-constexpr int PF_WARPS = 4;
-constexpr int PF_ROWS = 64;  // state rows per CTA, 16 per warp
+#ifndef GDN_PREFILL_WARPS
+#define GDN_PREFILL_WARPS 8  // a CTA covers 128 state rows: the per-chunk staging and normalisation serve more rows
+#endif
+constexpr int PF_WARPS = GDN_PREFILL_WARPS;
+constexpr int PF_ROWS = 16 * PF_WARPS;  // state rows per CTA, 16 per warp
 #ifndef GDN_PREFILL_TOKENS
 #define GDN_PREFILL_TOKENS 16
 #endif
 constexpr int PF_TC = GDN_PREFILL_TOKENS;  // tokens per staged chunk
 #ifndef GDN_PREFILL_MIN_BLOCKS
-#define GDN_PREFILL_MIN_BLOCKS 4  // CTAs per SM the register budget must allow
+#define GDN_PREFILL_MIN_BLOCKS 2  // CTAs per SM the register budget must allow (128 registers a thread)
 #endif
 
 template <typename ST, int DK>
