@@ -116,7 +116,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
 
     const int isz = dtype_size(p.in_dtype);
     auto raw = [&](int c) { return smem + (c & 1) * p.raw_bytes; };  // staged chunk c
-    float* kqn = reinterpret_cast<float*>(smem + p.off_kqn);     // [TC][2][DK] normalised k, q
+    // [TC][2][DK] normalised k, q, each row in lane order: the 4-element piece e4 of a lane's run cc sits at
+    // ((cc * VEC / 4 + e4) * LPR + pg) * 4, so the row loop's 16-byte reads are consecutive across lanes
+    float* kqn = reinterpret_cast<float*>(smem + p.off_kqn);
     float* qkb = reinterpret_cast<float*>(smem + p.off_qk);      // [TC] q.k
     float* vf = reinterpret_cast<float*>(smem + p.off_vf);       // [TC][PF_ROWS] v in FP32
     float* of = reinterpret_cast<float*>(smem + p.off_of);       // [TC][PF_ROWS] outputs
@@ -215,8 +217,10 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             for (int e = 0; e < DK / 32; ++e) {
                 kx[e] *= ik, qx[e] *= iq;
                 kq = fmaf(kx[e], qx[e], kq);
-                kqn[(t * 2) * DK + lane + 32 * e] = kx[e];
-                kqn[(t * 2 + 1) * DK + lane + 32 * e] = qx[e];
+                const int i = lane + 32 * e, run = i / C::VEC, within = i - run * C::VEC;
+                const int slot = (((run / C::LPR) * (C::VEC / 4) + within / 4) * C::LPR + run % C::LPR) * 4 + within % 4;
+                kqn[(t * 2) * DK + slot] = kx[e];
+                kqn[(t * 2 + 1) * DK + slot] = qx[e];
             }
             kq = group_sum<32>(kq);
             if (lane == 0) qkb[t] = kq;
@@ -234,8 +238,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
                 for (int cc = 0; cc < C::NC; ++cc) {
 #pragma unroll
                     for (int e = 0; e < C::VEC; e += 4) {
-                        const float4 kv = *reinterpret_cast<const float4*>(kqn + (t * 2) * DK + pos_of(cc) + e);
-                        const float4 qv = *reinterpret_cast<const float4*>(kqn + (t * 2 + 1) * DK + pos_of(cc) + e);
+                        const int slot = ((cc * (C::VEC / 4) + e / 4) * C::LPR + pg) * 4;
+                        const float4 kv = *reinterpret_cast<const float4*>(kqn + (t * 2) * DK + slot);
+                        const float4 qv = *reinterpret_cast<const float4*>(kqn + (t * 2 + 1) * DK + slot);
                         const int i = (cc * C::VEC + e) / 2;
                         k2[i] = make_float2(kv.x, kv.y), k2[i + 1] = make_float2(kv.z, kv.w);
                         q2[i] = make_float2(qv.x, qv.y), q2[i + 1] = make_float2(qv.z, qv.w);
