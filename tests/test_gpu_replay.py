@@ -153,6 +153,19 @@ def test_verify_and_rollback_small(T, L, sdt):
     H.check_state()
 
 
+@pytest.mark.parametrize("sdt", ["f32", "bf16"])
+def test_maximum_ring_window_and_head(sdt):
+    # the largest ring (L = 32), window (T = 8) and head (dk = 128, dv = 256) the entry points take
+    w = wl.Workload("mx", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=9, state_dtype=sdt, in_dtype="bf16", L=32, T=8,
+                    seed=27)
+    H = Harness(w)
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, 8, f"round {r}")
+        H.rollback(wl.accepted(w, r), 8)
+    H.window(wl.step_inputs(w.with_(T=1), 700), H.slots, 1, "step")
+    H.check_state()
+
+
 @pytest.mark.parametrize("force", [True, False])
 def test_flush(force):
     w = wl.Workload("fl", B=6, Hk=1, Hv=2, dk=128, dv=64, steps=1, state_dtype="bf16", in_dtype="bf16", L=8,
