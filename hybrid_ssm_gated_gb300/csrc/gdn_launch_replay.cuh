@@ -32,10 +32,13 @@ constexpr int replay_warps() {
 #define GDN_REPLAY_MIN_CHUNKS 6
 #endif
 
-// Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype).
-// Returns the total dynamic shared memory in bytes, or -1 if it cannot fit.
+// Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype, nchunk, mnchunk).
+// Returns the total dynamic shared memory in bytes, or -1 if it cannot fit. The chunk ring holds at
+// least one whole unit: a unit's head barrier completes only once every chunk of the unit is armed,
+// so a unit with more chunks than stages could never complete.
 template <int DK, int TMAX>
 int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
+    const int need = a.nchunk > a.mnchunk ? a.nchunk : a.mnchunk;
     const int in_sz = dtype_size(a.in_dtype);
     const int T = a.T, L = a.L;
     // head stage: meta | window q, k, v rows | ring keys | ring records | coefficient table
@@ -50,12 +53,15 @@ int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
         // mbarriers: 2 per chunk stage, 3 per head stage; a 4-byte counter per head stage
         return ns * CHUNK_BYTES + nh * a.head_bytes + sums_bytes + (2 * ns + 3 * nh) * 8 + align_up(nh * 4, 16);
     };
-    // deepest head ring (units in flight) that leaves GDN_REPLAY_MIN_CHUNKS chunk stages, then more
-    // chunk stages
+    // deepest head ring (units in flight) that leaves GDN_REPLAY_MIN_CHUNKS chunk stages (and at
+    // least a unit's), then more chunk stages
+    const int floor_ns = need > 2 ? need : 2;
     int ns = 0, nh = 0;
-    for (int min_ns = GDN_REPLAY_MIN_CHUNKS; min_ns >= 2 && !ns; min_ns -= 2)
-        for (int h = GDN_REPLAY_MAX_HEADS; h >= 2 && !ns; --h)
+    for (int min_ns = GDN_REPLAY_MIN_CHUNKS > floor_ns ? GDN_REPLAY_MIN_CHUNKS : floor_ns; min_ns >= floor_ns && !ns;
+         min_ns -= 2)
+        for (int h = GDN_REPLAY_MAX_HEADS; h >= 1 && !ns; --h)
             if (total(min_ns, h) <= smem_limit) ns = min_ns, nh = h;
+    if (!ns && total(floor_ns, 1) <= smem_limit) ns = floor_ns, nh = 1;
     if (!ns) return -1;
     while (ns < 12 && total(ns + 1, nh) <= smem_limit) ++ns;
     a.nstage = ns, a.nhead = nh;

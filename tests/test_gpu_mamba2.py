@@ -210,6 +210,16 @@ def test_verify_and_rollback_small(T, L, sdt):
     H.check_state()
 
 
+def test_verify_at_the_largest_ring_window_and_head():
+    w = wl.Workload("m2x", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=6, state_dtype="f32", in_dtype="bf16", L=32, T=8,
+                    seed=59)
+    H = M2Harness(w)
+    for r in range(w.steps):
+        H.window(wl.mamba2_step_inputs(w, r), H.slots, 8, f"round {r}")
+        H.rollback(wl.accepted(w, r), 8)
+    H.check_state()
+
+
 def test_padding_in_replay():
     w = wl.Workload("m2q", B=6, Hk=1, Hv=2, dk=32, dv=32, steps=6, state_dtype="f32", in_dtype="f32", L=4, seed=58)
     H = M2Harness(w)
