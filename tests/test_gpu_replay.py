@@ -248,6 +248,19 @@ def test_read_copy_small_all_units(rdt, T, L):
     H.check_state()
 
 
+@pytest.mark.parametrize("T", [1, 4])
+def test_read_copy_large_head(T):
+    # 128 x 256 heads: a fold unit streams 8 master chunks, twice a copy unit's
+    w = wl.Workload("rcl", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=8, state_dtype="f32", in_dtype="bf16", L=8, T=T,
+                    seed=42)
+    H = Harness(w, read_dtype="bf16")
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, T, f"round {r}")
+        if T > 1:
+            H.rollback(wl.accepted(w, r), T)
+    H.check_state()
+
+
 @pytest.mark.slow
 def test_read_copy_b256_sampled():
     w = wl.WORKLOADS["replay_b256_f32"]
