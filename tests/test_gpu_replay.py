@@ -166,6 +166,18 @@ def test_maximum_ring_window_and_head(sdt):
     H.check_state()
 
 
+@pytest.mark.parametrize("dk,dv", [(32, 96), (128, 32), (64, 256), (32, 32)])
+@pytest.mark.parametrize("T", [3, 8])
+def test_verify_other_head_shapes(dk, dv, T):
+    w = wl.Workload("vh", B=5, Hk=2, Hv=4, dk=dk, dv=dv, steps=6, state_dtype="f32", in_dtype="bf16", L=16, T=T,
+                    seed=28)
+    H = Harness(w)
+    for r in range(w.steps):
+        H.window(wl.step_inputs(w, r), H.slots, T, f"round {r}")
+        H.rollback(wl.accepted(w, r), T)
+    H.check_state()
+
+
 @pytest.mark.parametrize("force", [True, False])
 def test_flush(force):
     w = wl.Workload("fl", B=6, Hk=1, Hv=2, dk=128, dv=64, steps=1, state_dtype="bf16", in_dtype="bf16", L=8,
