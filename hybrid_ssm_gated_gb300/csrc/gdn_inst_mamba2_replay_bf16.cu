@@ -8,9 +8,9 @@ namespace gdn {
 cudaError_t dispatch_mamba2_replay_bf16(int dk, int tmax, ReplayArgs& a, cudaStream_t s, bool& too_big) {
 #define GDN_REP(DK)                                                                          \
     if (dk == DK) {                                                                          \
-        if (tmax == 1) return launch_replay<__nv_bfloat16, DK, 1, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
-        if (tmax == 4) return launch_replay<__nv_bfloat16, DK, 4, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
-        if (tmax == 8) return launch_replay<__nv_bfloat16, DK, 8, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 1) return launch_replay_io<__nv_bfloat16, DK, 1, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 4) return launch_replay_io<__nv_bfloat16, DK, 4, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 8) return launch_replay_io<__nv_bfloat16, DK, 8, __nv_bfloat16, RULE_MAMBA2>(a, s, too_big);    \
     }
     GDN_REP(32)
     GDN_REP(64)

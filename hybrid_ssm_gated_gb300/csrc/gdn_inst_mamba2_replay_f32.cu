@@ -8,9 +8,9 @@ namespace gdn {
 cudaError_t dispatch_mamba2_replay_f32(int dk, int tmax, ReplayArgs& a, cudaStream_t s, bool& too_big) {
 #define GDN_REP(DK)                                                                          \
     if (dk == DK) {                                                                          \
-        if (tmax == 1) return launch_replay<float, DK, 1, float, RULE_MAMBA2>(a, s, too_big);    \
-        if (tmax == 4) return launch_replay<float, DK, 4, float, RULE_MAMBA2>(a, s, too_big);    \
-        if (tmax == 8) return launch_replay<float, DK, 8, float, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 1) return launch_replay_io<float, DK, 1, float, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 4) return launch_replay_io<float, DK, 4, float, RULE_MAMBA2>(a, s, too_big);    \
+        if (tmax == 8) return launch_replay_io<float, DK, 8, float, RULE_MAMBA2>(a, s, too_big);    \
     }
     GDN_REP(32)
     GDN_REP(64)

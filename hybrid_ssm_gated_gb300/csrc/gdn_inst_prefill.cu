@@ -5,9 +5,9 @@
 
 namespace gdn {
 
-template <typename ST, int DK>
+template <typename ST, int DK, int IO>
 cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
-    auto kern = prefill_kernel<ST, DK>;
+    auto kern = prefill_kernel<ST, DK, IO>;
     const int isz = dtype_size(a.in_dtype);
     a.raw_bytes = PF_TC * (2 * DK + PF_ROWS) * isz;
     a.off_kqn = 2 * a.raw_bytes;
@@ -25,12 +25,19 @@ cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// The bf16-in / fp32-out instantiation when the arguments match it, the generic one otherwise.
+template <typename ST, int DK>
+cudaError_t launch_prefill_io(PrefillArgs& a, cudaStream_t stream) {
+    if (io_mode(a.in_dtype, a.out_dtype) == IO_BF16_F32) return launch_prefill<ST, DK, IO_BF16_F32>(a, stream);
+    return launch_prefill<ST, DK, IO_ANY>(a, stream);
+}
+
 cudaError_t dispatch_prefill(int state_dtype, int dk, PrefillArgs& a, cudaStream_t s) {
-#define GDN_PF(CODE, ST)                                    \
-    if (state_dtype == CODE) {                              \
-        if (dk == 32) return launch_prefill<ST, 32>(a, s);  \
-        if (dk == 64) return launch_prefill<ST, 64>(a, s);  \
-        if (dk == 128) return launch_prefill<ST, 128>(a, s); \
+#define GDN_PF(CODE, ST)                                       \
+    if (state_dtype == CODE) {                                 \
+        if (dk == 32) return launch_prefill_io<ST, 32>(a, s);   \
+        if (dk == 64) return launch_prefill_io<ST, 64>(a, s);   \
+        if (dk == 128) return launch_prefill_io<ST, 128>(a, s); \
     }
     GDN_PF(GDN_F32, float)
     GDN_PF(GDN_BF16, __nv_bfloat16)

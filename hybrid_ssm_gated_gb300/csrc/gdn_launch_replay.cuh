@@ -73,11 +73,11 @@ int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
 
 // ST: the checkpoint steps read; MT: the one folds update (a wider master, or ST);
 // RULE: the recurrence (gated delta rule or Mamba2).
-template <typename ST, int DK, int TMAX, typename MT = ST, int RULE = RULE_GDN>
+template <typename ST, int DK, int TMAX, typename MT = ST, int RULE = RULE_GDN, int IO = IO_ANY>
 cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
     constexpr int NCW = replay_warps<TMAX>();
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
-    auto kern = replay_kernel<ST, DK, TMAX, NCW, MT, RULE>;
+    auto kern = replay_kernel<ST, DK, TMAX, NCW, MT, RULE, IO>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;
@@ -90,6 +90,14 @@ cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
     const int grid = units < di.sms * bps ? units : di.sms * bps;
     kern<<<grid, C::THREADS, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+// The bf16-in / fp32-out instantiation when the arguments match it, the generic one otherwise.
+template <typename ST, int DK, int TMAX, typename MT = ST, int RULE = RULE_GDN>
+cudaError_t launch_replay_io(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
+    if (io_mode(a.in_dtype, a.out_dtype) == IO_BF16_F32)
+        return launch_replay<ST, DK, TMAX, MT, RULE, IO_BF16_F32>(a, stream, too_big);
+    return launch_replay<ST, DK, TMAX, MT, RULE, IO_ANY>(a, stream, too_big);
 }
 
 }  // namespace gdn

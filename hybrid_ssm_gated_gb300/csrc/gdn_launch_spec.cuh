@@ -37,11 +37,11 @@ int spec_layout(SpecArgs& a, int smem_limit) {
     return total(ns, nh);
 }
 
-template <typename ST, int DK, int TMAX>
+template <typename ST, int DK, int TMAX, int IO>
 cudaError_t launch_spec(SpecArgs& a, cudaStream_t stream, bool& too_big) {
     constexpr int NCW = spec_warps<TMAX>();
     using C = SpecCfg<ST, DK, TMAX, NCW>;
-    auto kern = spec_kernel<ST, DK, TMAX, NCW>;
+    auto kern = spec_kernel<ST, DK, TMAX, NCW, IO>;
     DeviceInfo di;
     cudaError_t e = device_info(di);
     if (e != cudaSuccess) return e;
@@ -56,13 +56,21 @@ cudaError_t launch_spec(SpecArgs& a, cudaStream_t stream, bool& too_big) {
     return cudaGetLastError();
 }
 
+// The bf16-in / fp32-out instantiation when the arguments match it, the generic one otherwise.
+template <typename ST, int DK, int TMAX>
+cudaError_t launch_spec_io(SpecArgs& a, cudaStream_t stream, bool& too_big) {
+    if (io_mode(a.in_dtype, a.out_dtype) == IO_BF16_F32)
+        return launch_spec<ST, DK, TMAX, IO_BF16_F32>(a, stream, too_big);
+    return launch_spec<ST, DK, TMAX, IO_ANY>(a, stream, too_big);
+}
+
 // The window size's kernel (tmax 4 or 8) for one state type, by dk.
 template <typename ST>
 cudaError_t dispatch_spec_t(int dk, int tmax, SpecArgs& a, cudaStream_t s, bool& too_big) {
 #define GDN_SPEC(DK)                                                     \
     if (dk == DK) {                                                      \
-        if (tmax == 4) return launch_spec<ST, DK, 4>(a, s, too_big);     \
-        if (tmax == 8) return launch_spec<ST, DK, 8>(a, s, too_big);     \
+        if (tmax == 4) return launch_spec_io<ST, DK, 4>(a, s, too_big);  \
+        if (tmax == 8) return launch_spec_io<ST, DK, 8>(a, s, too_big);  \
     }
     GDN_SPEC(32)
     GDN_SPEC(64)

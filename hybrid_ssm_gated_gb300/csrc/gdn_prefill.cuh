@@ -36,6 +36,7 @@
 #pragma once
 
 #include "gdn_device.cuh"
+#include "gdn_io.cuh"
 
 namespace gdn {
 
@@ -87,9 +88,10 @@ struct PrefillCfg {
     static_assert(DK % E == 0 && 16 % RPP == 0 && 2 * PASSES == LPR, "unsupported dk");
 };
 
-template <typename ST, int DK>
+template <typename ST, int DK, int IO = IO_ANY>
 __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill_kernel(const PrefillArgs p) {
     using C = PrefillCfg<ST, DK>;
+    const int in_dt = io_in<IO>(p.in_dtype), out_dt = io_out<IO>(p.out_dtype);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x % p.row_blocks;
@@ -108,13 +110,13 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         if (slot >= p.num_slots && threadIdx.x == 0 && rb == 0) set_error(p.dev_err, GDN_DEVERR_SLOT);
         for (int i = threadIdx.x; i < T * nrows; i += blockDim.x) {
             const int t = i / nrows, r = i - t * nrows;
-            store_elem(p.out, ((int64_t)(t0 + t) * p.Hv + h) * p.dv + row0 + r, p.out_dtype, 0.f);
+            store_elem(p.out, ((int64_t)(t0 + t) * p.Hv + h) * p.dv + row0 + r, out_dt, 0.f);
         }
         return;
     }
     if (T == 0) return;
 
-    const int isz = dtype_size(p.in_dtype);
+    const int isz = dtype_size(in_dt);
     auto raw = [&](int c) { return smem + (c & 1) * p.raw_bytes; };  // staged chunk c
     // [TC][2][DK] normalised k, q, each row in lane order: the 4-element piece e4 of a lane's run cc sits at
     // ((cc * VEC / 4 + e4) * LPR + pg) * 4, so the row loop's 16-byte reads are consecutive across lanes
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         al = 0.f, be = 0.f;
         if (threadIdx.x < PF_TC && t < T) {
             const int64_t gi = (int64_t)(t0 + t) * p.Hv + h;
-            gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype), load_elem(p.b, gi, p.in_dtype), al, be);
+            gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, in_dt), load_elem(p.b, gi, in_dt), al, be);
         }
     };
 
@@ -206,8 +208,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             float ssk = 0.f, ssq = 0.f;
 #pragma unroll
             for (int e = 0; e < DK / 32; ++e) {
-                kx[e] = load_elem(src + (PF_TC + t) * qbytes, lane + 32 * e, p.in_dtype);
-                qx[e] = load_elem(src + t * qbytes, lane + 32 * e, p.in_dtype);
+                kx[e] = load_elem(src + (PF_TC + t) * qbytes, lane + 32 * e, in_dt);
+                qx[e] = load_elem(src + t * qbytes, lane + 32 * e, in_dt);
                 ssk = fmaf(kx[e], kx[e], ssk), ssq = fmaf(qx[e], qx[e], ssq);
             }
             const float ik = rsqrtf(group_sum<32>(ssk) + 1e-6f);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             kq = group_sum<32>(kq);
             if (lane == 0) qkb[t] = kq;
             for (int r = lane; r < nrows; r += 32)
-                vf[t * PF_ROWS + r] = load_elem(src + 2 * PF_TC * qbytes + t * PF_ROWS * isz, r, p.in_dtype);
+                vf[t * PF_ROWS + r] = load_elem(src + 2 * PF_TC * qbytes + t * PF_ROWS * isz, r, in_dt);
         }
         __syncthreads();  // the table is complete
 
@@ -328,14 +330,14 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             const int t = i / q4, r = (i - t * q4) * 4;
             const float4 o = *reinterpret_cast<const float4*>(of + t * PF_ROWS + r);
             const int64_t oi = ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0 + r;
-            if (p.out_dtype == GDN_F32) {
+            if (out_dt == GDN_F32) {
                 *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = o;
             } else {
                 const float ov[4] = {o.x, o.y, o.z, o.w};
                 uint32_t w[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
-                    w[e] = p.out_dtype == GDN_BF16 ? pack_bf16x2(ov[2 * e], ov[2 * e + 1])
+                    w[e] = out_dt == GDN_BF16 ? pack_bf16x2(ov[2 * e], ov[2 * e + 1])
                                                    : pack_f16x2(ov[2 * e], ov[2 * e + 1]);
                 *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + oi) = make_uint2(w[0], w[1]);
             }

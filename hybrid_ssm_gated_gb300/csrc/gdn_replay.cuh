@@ -73,6 +73,7 @@
 
 #include "gdn_decode.cuh"
 #include "gdn_device.cuh"
+#include "gdn_io.cuh"
 
 namespace gdn {
 
@@ -198,9 +199,10 @@ __device__ __forceinline__ void reduce_scatter_values(float (&x)[V], int g) {
 
 // ST: the checkpoint that steps and windows read (the read copy in the two-checkpoint mode);
 // MT: the checkpoint that folds read and write (ST itself with one checkpoint).
-template <typename ST, int DK, int TMAX, int NCW, typename MT = ST, int RULE = RULE_GDN>
+template <typename ST, int DK, int TMAX, int NCW, typename MT = ST, int RULE = RULE_GDN, int IO = IO_ANY>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayArgs p) {
     using C = ReplayCfg<ST, DK, TMAX, NCW>;
+    const int in_dt = io_in<IO>(p.in_dtype), out_dt = io_out<IO>(p.out_dtype);
     constexpr bool MIXED = !std::is_same<ST, MT>::value;
     constexpr int MROW_BYTES = DK * (int)sizeof(MT);  // a master row
     extern __shared__ __align__(128) unsigned char smem[];
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
     __syncthreads();
 
     const int total = p.B * p.Hv;
-    const int in_sz = dtype_size(p.in_dtype);
+    const int in_sz = dtype_size(in_dt);
     const int group = p.Hv / p.Hk;
     const int T = p.T, L = p.L;
     const int rec_floats = 4 + p.dv;
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         for (int t = 0; t < TMAX; ++t) {
                             if (t < T) {
                                 const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
-                                rule_gates<RULE>(p.A_log[h], p.dt_bias[h], p.a, p.b, gi, p.in_dtype, al[t], be[t]);
+                                rule_gates<RULE>(p.A_log[h], p.dt_bias[h], p.a, p.b, gi, in_dt, al[t], be[t]);
                             }
                         }
                     } else {
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
             if (slot == -1) {
                 for (int x = cw * 32 + lane; x < T * p.dv; x += NCW * 32) {
                     const int t = x / p.dv, j = x - t * p.dv;
-                    store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, 0.f);
+                    store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt, 0.f);
                 }
             }
             __syncwarp();
@@ -481,8 +483,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 if (t < T) {
 #pragma unroll
                     for (int cc = 0; cc < C::NC; ++cc) {
-                        load_run<C::VEC>(head + p.off_wk + t * DK * in_sz, pos_of(cc), p.in_dtype, xk + cc * C::VEC);
-                        load_run<C::VEC>(head + p.off_wq + t * DK * in_sz, pos_of(cc), p.in_dtype, xq + cc * C::VEC);
+                        load_run<C::VEC>(head + p.off_wk + t * DK * in_sz, pos_of(cc), in_dt, xk + cc * C::VEC);
+                        load_run<C::VEC>(head + p.off_wq + t * DK * in_sz, pos_of(cc), in_dt, xq + cc * C::VEC);
                     }
                     ikw[t] = 1.f;
                     if constexpr (RULE == RULE_GDN) {
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         float raw[C::E];
 #pragma unroll
                         for (int cc = 0; cc < C::NC; ++cc)
-                            load_run<C::VEC>(rk + xc * DK * in_sz, pos_of(cc), p.in_dtype, raw + cc * C::VEC);
+                            load_run<C::VEC>(rk + xc * DK * in_sz, pos_of(cc), in_dt, raw + cc * C::VEC);
                         const float ikf = rec[xc * rec_floats + 2];
 #pragma unroll
                         for (int e = 0; e < C::E / 2; ++e) kx[e] = make_float2(raw[2 * e] * ikf, raw[2 * e + 1] * ikf);
@@ -638,8 +640,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         float k0[C::E], k1[C::E];
 #pragma unroll
                         for (int cc = 0; cc < C::NC; ++cc) {
-                            load_run<C::VEC>(rk + f * DK * in_sz, pos_of(cc), p.in_dtype, k0 + cc * C::VEC);
-                            load_run<C::VEC>(rk + (two ? f + 1 : f) * DK * in_sz, pos_of(cc), p.in_dtype, k1 + cc * C::VEC);
+                            load_run<C::VEC>(rk + f * DK * in_sz, pos_of(cc), in_dt, k0 + cc * C::VEC);
+                            load_run<C::VEC>(rk + (two ? f + 1 : f) * DK * in_sz, pos_of(cc), in_dt, k1 + cc * C::VEC);
                         }
 #pragma unroll
                         for (int r = 0; r < NR; ++r) {
@@ -734,10 +736,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                     const float Y = group_sum<C::LPR>(u2.x + u2.y);
                                     const float Z = group_sum<C::LPR>(v2.x + v2.y) * al;
                                     const int j = jr[r];
-                                    const float vj = load_elem(head + p.off_wv, j, p.in_dtype);
+                                    const float vj = load_elem(head + p.off_wv, j, in_dt);
                                     const float ww = RULE == RULE_GDN ? be * (vj - al * Y) : be * vj;
                                     if (pg == 0) {
-                                        store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype,
+                                        store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, out_dt,
                                                    fmaf(dskip, vj, fmaf(qk, ww, Z)));
                                         p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                                     }
@@ -802,9 +804,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 }
                                 Y += Y1, Z += Z1;
                             }
-                            const float vj = load_elem(head + p.off_wv, j, p.in_dtype);
+                            const float vj = load_elem(head + p.off_wv, j, in_dt);
                             const float ww = RULE == RULE_GDN ? be * (vj - al * Y) : be * vj;
-                            store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, p.out_dtype,
+                            store_elem(p.out, ((int64_t)b * p.Hv + h) * p.dv + j, out_dt,
                                        fmaf(dskip, vj, fmaf(qk, ww, Z)));
                             p.ring_rec[(unit_ring + pos0 % L) * rec_floats + 4 + j] = ww;
                         }
@@ -881,7 +883,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
 #pragma unroll
                             for (int x = 0; x < TMAX; ++x) {
                                 if (x < T) {
-                                    const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, p.in_dtype);
+                                    const float vx = load_elem(head + p.off_wv + x * p.dv * in_sz, j, in_dt);
                                     const float wx = RULE == RULE_GDN ? meta->beta[x] * (vx - meta->alpha[x] * y[x])
                                                                       : meta->beta[x] * vx;
                                     wcol[(int64_t)ri * rec_floats] = wx;
@@ -899,8 +901,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 if (t < T) {
                                     float o = z[t];
                                     if constexpr (RULE == RULE_MAMBA2)
-                                        o = fmaf(dskip, load_elem(head + p.off_wv + t * p.dv * in_sz, j, p.in_dtype), o);
-                                    store_elem(p.out, ob + t * ot, p.out_dtype, o);
+                                        o = fmaf(dskip, load_elem(head + p.off_wv + t * p.dv * in_sz, j, in_dt), o);
+                                    store_elem(p.out, ob + t * ot, out_dt, o);
                                 }
                         }
                         __syncwarp();  // the tile is free for the next item

@@ -30,6 +30,7 @@
 
 #include "gdn_decode.cuh"
 #include "gdn_device.cuh"
+#include "gdn_io.cuh"
 
 namespace gdn {
 
@@ -80,9 +81,10 @@ struct SpecCfg {
     static_assert(E % VEC == 0 && DK % E == 0 && LPR >= 2 && LPR <= 32, "unsupported dk");
 };
 
-template <typename ST, int DK, int TMAX, int NCW>
+template <typename ST, int DK, int TMAX, int NCW, int IO = IO_ANY>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs p) {
     using C = SpecCfg<ST, DK, TMAX, NCW>;
+    const int in_dt = io_in<IO>(p.in_dtype), out_dt = io_out<IO>(p.out_dtype);
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* chunks = smem;
     unsigned char* heads = smem + p.heads_off;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
     __syncthreads();
 
     const int total = p.B * p.Hv;
-    const int in_sz = dtype_size(p.in_dtype);
+    const int in_sz = dtype_size(in_dt);
     const int group = p.Hv / p.Hk;
     const int T = p.T;
 
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                     for (int t = 0; t < TMAX; ++t) {
                         if (t < T) {
                             const int64_t gi = ((int64_t)b * T + t) * p.Hv + h;
-                            gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, p.in_dtype),
-                                  load_elem(p.b, gi, p.in_dtype), al[t], be[t]);
+                            gates(p.A_log[h], p.dt_bias[h], load_elem(p.a, gi, in_dt),
+                                  load_elem(p.b, gi, in_dt), al[t], be[t]);
                         }
                     }
                 }
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
         if (src < 0) {
             for (int x = cw * 32 + lane; x < T * p.dv; x += NCW * 32) {
                 const int t = x / p.dv, j = x - t * p.dv;
-                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype, 0.f);
+                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt, 0.f);
             }
         } else {
             // the window's keys and queries, normalised, at this lane's key positions; q_t.k_t
@@ -269,8 +271,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                 if (t < T) {
 #pragma unroll
                     for (int cc = 0; cc < C::NC; ++cc) {
-                        load_run<C::VEC>(head + p.off_k + t * DK * in_sz, pos_of(cc), p.in_dtype, xk + cc * C::VEC);
-                        load_run<C::VEC>(head + p.off_q + t * DK * in_sz, pos_of(cc), p.in_dtype, xq + cc * C::VEC);
+                        load_run<C::VEC>(head + p.off_k + t * DK * in_sz, pos_of(cc), in_dt, xk + cc * C::VEC);
+                        load_run<C::VEC>(head + p.off_q + t * DK * in_sz, pos_of(cc), in_dt, xq + cc * C::VEC);
                     }
                     float ssk = 0.f, ssq = 0.f;
 #pragma unroll
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                             const float u = group_sum<C::LPR>(u2.x + u2.y);
                             const float pq = group_sum<C::LPR>(p2.x + p2.y);
                             const float alpha = meta->alpha[t], beta = meta->beta[t];
-                            const float vj = load_elem(head + p.off_v + t * p.dv * in_sz, j, p.in_dtype);
+                            const float vj = load_elem(head + p.off_v + t * p.dv * in_sz, j, in_dt);
                             const float delta = beta * (vj - alpha * u);
                             const float2 al2 = make_float2(alpha, alpha), d2 = make_float2(delta, delta);
 #pragma unroll
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                                 s[2 * e] = r2.x, s[2 * e + 1] = r2.y;
                             }
                             if (pg == 0)
-                                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, p.out_dtype,
+                                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt,
                                            fmaf(alpha, pq, qk[t] * delta));
                             const int d = meta->dst[t];
                             if (d >= 0) {  // this token's state copy, rounded once
