@@ -172,14 +172,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                 if (s_i >= 0) {
                     const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
                     const int64_t qrow = (int64_t)b * p.Hk + kh;
-                    if (lane == 0)
-                        bulk_load(head + C::OFF_Q, static_cast<const char*>(p.q) + qrow * qbytes, qbytes, &hfull[hs]);
-                    else if (lane == 1)
-                        bulk_load(head + C::OFF_K, static_cast<const char*>(p.k) + qrow * qbytes, qbytes, &hfull[hs]);
-                    else if (lane == 2)
-                        bulk_load(head + C::OFF_V, static_cast<const char*>(p.v) + (int64_t)unit * vbytes, vbytes,
-                                  &hfull[hs]);
-                    // at most NS lanes at a time, so no lane waits for a stage another lane is about to fill
+                    // the q/k/v rows first, in one convergent copy instruction (lanes 0-2)
+                    {
+                        const char* src = lane == 0   ? static_cast<const char*>(p.q) + qrow * qbytes
+                                          : lane == 1 ? static_cast<const char*>(p.k) + qrow * qbytes
+                                                      : static_cast<const char*>(p.v) + (int64_t)unit * vbytes;
+                        unsigned char* dst = head + (lane == 0 ? C::OFF_Q : lane == 1 ? C::OFF_K : C::OFF_V);
+                        if (lane < 3) bulk_load(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs]);
+                    }
+                    // then the chunks, each lane's as soon as its stage is free (a wait for every stage
+                    // first delays the early chunks); at most NS lanes at a time, so no lane waits for a
+                    // stage another lane is about to fill
                     for (int c0 = 0; c0 < p.nchunk && ok; c0 += NS) {
                         const int c = c0 + lane;
                         if (lane < NS && c < p.nchunk) {
