@@ -29,8 +29,8 @@
 //    lane per unit). Per unit it bulk-copies the window's q/k/v rows and the
 //    buffered ring entries (keys, records) into an NH-deep head ring and S0 in
 //    16 KB chunks into an NS-deep chunk ring, one copy per lane, in one
-//    convergent copy instruction (a window over a unit of more than two
-//    chunks sends its rows and ring ahead in one, then the chunks): a thread
+//    convergent copy instruction (a large unit sends its rows and ring ahead
+//    in one, then the chunks): a thread
 //    issues a bulk copy only every ~0.25 us, but the lanes of one instruction
 //    issue together.
 //  - Every consumer warp visits every unit in order. A unit's state rows are
@@ -340,15 +340,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                  ((int64_t)s_i * p.Hv + h) * p.dv * (fm ? MROW_BYTES : C::ROW_BYTES);
                 // Copies: lanes 0..3T-1 the window's q/k/v rows, the next four up to two ring ranges (keys,
                 // records), the others S0 chunks, at most NS of them at a time so that no lane waits for a
-                // stage another lane is about to fill. A window over a unit of more than two chunks issues
-                // its rows and ring first, then each chunk as soon as its stage is free: waiting for all of
-                // them would hold the rows back by up to a unit's worth of consumption (T = 4 windows over
-                // fp32 128 x 128 states: 11% faster). Otherwise every copy of the unit goes out in one
-                // convergent bulk-copy instruction once its chunk stages are free (more rounds only when
-                // the chunks do not fit): small units are bound by the producer's instructions per unit.
+                // stage another lane is about to fill. A unit of more than two chunks issues its rows and
+                // ring first, then each chunk as soon as its stage is free: waiting for all of them would
+                // hold the rows back by up to a unit's worth of consumption (T = 4 windows over fp32
+                // 128 x 128 states: 11% faster, single tokens 2%). Otherwise every copy of the unit goes
+                // out in one convergent bulk-copy instruction once its chunk stages are free (more rounds
+                // only when the chunks do not fit). The split is compiled only where it can pay: in the
+                // single-token kernels of small units, even untaken, it cost up to 17%.
+                constexpr bool SPLIT = TMAX > 1 || (RULE == RULE_GDN && std::is_same<ST, float>::value && !MIXED);
                 const int hj = 3 * T + 4;
                 bool split = false;
-                if constexpr (TMAX > 1) split = nck > 2;
+                if constexpr (SPLIT) split = nck > 2;
                 for (int c0 = 0, round = 0; ok && (round == 0 || c0 < nck); ++round) {
                     const int cl0 = split ? 32 : round == 0 ? hj : 0;  // first chunk lane of this round
                     const int per = min(NS, 32 - cl0);                 // chunk lanes of this round
