@@ -29,7 +29,7 @@ constexpr int replay_warps() {
 #define GDN_REPLAY_MAX_HEADS 6
 #endif
 #ifndef GDN_REPLAY_MIN_CHUNKS
-#define GDN_REPLAY_MIN_CHUNKS 6
+#define GDN_REPLAY_MIN_CHUNKS 8
 #endif
 
 // Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype, nchunk, mnchunk).
