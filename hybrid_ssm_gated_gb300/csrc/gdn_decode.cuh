@@ -83,7 +83,11 @@ struct DecodeCfg {
     static constexpr int OFF_V = OFF_K + DK * 4;
     static constexpr int HEAD = align_up(OFF_V + DV_MAX * 4, 128);
     static constexpr int SMEM = NS * CHUNK_BYTES + NH * HEAD + (2 * NS + 2 * NH) * 8;
-    static constexpr int THREADS = (NCW + 1) * 32;
+    // producer warps: units of a 16-bit state are small enough that one warp's per-unit issue latency
+    // (about 0.75 us) bounds the step, so two warps take alternate units
+    static constexpr int NP = sizeof(ST) == 2 ? 2 : 1;
+    static_assert(NH % NP == 0, "each head stage is filled by one producer warp");
+    static constexpr int THREADS = (NCW + NP) * 32;
     // warps per unit: a unit's passes are dealt over UW warps, the NG = NCW / UW groups taking
     // units in turn
     static constexpr int UW_ = RULE == RULE_GDN ? GDN_DECODE_UNIT_WARPS : GDN_DECODE_UNIT_WARPS_MAMBA2;
@@ -94,7 +98,7 @@ struct DecodeCfg {
 };
 
 template <typename ST, int DK, int NCW, int NS, int NH, int RULE = RULE_GDN>
-__global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) decode_kernel(const DecodeArgs p) {
     using C = DecodeCfg<ST, DK, NCW, NS, NH, RULE>;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* chunks = smem;
@@ -117,13 +121,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
     const int in_sz = dtype_size(p.in_dtype);
     const int group = p.Hv / p.Hk;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- producer
+    if (warp < C::NP) {
+        // ---------------------------------------------------------------- producer(s)
+        // With NP warps, warp w provisions units n = w (mod NP). Unit n's chunks take the fills after
+        // those of every earlier valid unit, whichever warp issued them; both warps count the valid
+        // units of every batch. A warp waits for a chunk stage only after the head stage of its unit
+        // was released, i.e. after the consumers finished unit n - NH: every fill older than one round
+        // of the ring has then been consumed, so the parity wait cannot alias.
         const uint64_t pol = policy_evict_first();
         const uint32_t qbytes = DK * in_sz, vbytes = p.dv * in_sz;
         const uint32_t cbytes = p.rows * C::ROW_BYTES;
-        uint32_t m = 0;   // chunk fills issued
-        uint32_t nh = 0;  // head fills issued
+        uint32_t m = 0;   // chunk fills issued (one producer: all; several: up to the last one this warp issued)
+        uint32_t nh = 0;  // head fills issued (likewise)
+        uint32_t vb = 0;  // valid units in earlier batches
         int n = 0;        // units visited
         bool ok = true;
         for (int n0 = 0; ok && blockIdx.x + n0 * gridDim.x < total; n0 += 32) {
@@ -141,6 +151,67 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
                     rule_gates<RULE>(p.A_log[h], p.dt_bias[h], p.a, p.b, my_unit, p.in_dtype, alpha, beta);
                     if constexpr (RULE == RULE_MAMBA2) dskip = p.D[h];
                 }
+            }
+            if constexpr (C::NP > 1) {
+                const unsigned valid = __ballot_sync(FULL_MASK, slot >= 0);
+                for (int i = warp; i < 32; i += C::NP) {
+                    n = n0 + i;
+                    const int unit = blockIdx.x + n * gridDim.x;
+                    if (unit >= total) break;
+                    const int s_i = __shfl_sync(FULL_MASK, slot, i);
+                    const float al = __shfl_sync(FULL_MASK, alpha, i);
+                    const float be = __shfl_sync(FULL_MASK, beta, i);
+                    const float dsk = RULE == RULE_MAMBA2 ? __shfl_sync(FULL_MASK, dskip, i) : 0.f;
+                    const int hs = n % NH;
+                    unsigned char* head = heads + hs * C::HEAD;
+                    if (lane == 0) {
+                        if (n >= NH) ok = mbar_wait(&hempty[hs], ((n / NH) + 1) & 1);
+                        if (ok) {
+                            reinterpret_cast<int*>(head)[0] = s_i;
+                            reinterpret_cast<float*>(head)[1] = al;
+                            reinterpret_cast<float*>(head)[2] = be;
+                            if constexpr (RULE == RULE_MAMBA2) reinterpret_cast<float*>(head)[3] = dsk;
+                            if (s_i >= 0)
+                                mbar_arrive_expect_tx(&hfull[hs], 2 * qbytes + vbytes);
+                            else
+                                mbar_arrive(&hfull[hs]);
+                        }
+                    }
+                    ok = __shfl_sync(FULL_MASK, ok, 0);
+                    if (!ok) break;
+                    nh = n + 1;
+                    if (s_i < 0) continue;
+                    const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
+                    const int64_t qrow = (int64_t)b * p.Hk + kh;
+                    {
+                        const char* src = lane == 0   ? static_cast<const char*>(p.q) + qrow * qbytes
+                                          : lane == 1 ? static_cast<const char*>(p.k) + qrow * qbytes
+                                                      : static_cast<const char*>(p.v) + (int64_t)unit * vbytes;
+                        unsigned char* dst = head + (lane == 0 ? C::OFF_Q : lane == 1 ? C::OFF_K : C::OFF_V);
+                        if (lane < 3) bulk_load(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs]);
+                    }
+                    // this unit's first fill: after those of the valid units before it
+                    const uint32_t m0 = (vb + __popc(valid & ((1u << i) - 1u))) * (uint32_t)p.nchunk;
+                    for (int c0 = 0; c0 < p.nchunk && ok; c0 += NS) {
+                        const int c = c0 + lane;
+                        if (lane < NS && c < p.nchunk) {
+                            const uint32_t mc = m0 + c;
+                            const int cs = mc % NS;
+                            ok = mc < NS || mbar_wait(&cempty[cs], ((mc / NS) + 1) & 1);
+                            if (ok) {
+                                const char* src = static_cast<const char*>(p.pool) +
+                                                  ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)c * cbytes;
+                                mbar_arrive_expect_tx(&cfull[cs], cbytes);
+                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                            }
+                        }
+                        ok = __all_sync(FULL_MASK, ok);
+                    }
+                    m = m0 + p.nchunk;
+                    if (!ok) break;
+                }
+                vb += __popc(valid);
+                continue;
             }
             for (int i = 0; i < 32; ++i, ++n) {
                 const int unit = blockIdx.x + n * gridDim.x;
@@ -213,7 +284,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) decode_kernel(const DecodeA
     }
 
     // -------------------------------------------------------------------- consumers
-    const int cw = warp - 1;
+    const int cw = warp - C::NP;
     const int pg = lane % C::LPR;        // lane's position within its row group
     const int rsub = lane / C::LPR;      // row within the warp pass
     const int passes = p.rows / C::RPP;  // warp passes per chunk
