@@ -13,8 +13,9 @@
 //
 // Kernel shape: persistent CTAs over (sequence, value head) units, one
 // producer warp + NCW consumer warps.
-//  - The producer warp fetches slot indices and gates for 32 units at a time
-//    (one lane per unit), then streams each unit's state in 16 KB chunks
+//  - The producer warp (two, taking alternate units, for 16-bit states)
+//    fetches slot indices and gates for 32 units at a time (one lane per
+//    unit), then streams each unit's state in 16 KB chunks
 //    into an NS-deep shared-memory ring with bulk copies on the TMA engine
 //    (cp.async.bulk + mbarrier transaction counts), together with the unit's
 //    q/k/v rows into an NH-deep "head" ring; a unit's copies are spread over
