@@ -108,6 +108,20 @@ def test_padding_and_out_of_range_slots():
         assert same == (s not in (3, 0, 7)), f"slot {s}"
 
 
+@pytest.mark.parametrize("sdt", ["bf16", "f16"])
+def test_padding_over_several_batches(sdt):
+    """160 x 32 = 5,120 units: more than 32 per CTA of a 152-CTA grid, so CTAs take a second batch of units.
+    A third of the sequences are padding and a seventh out of range, so the valid units before a unit differ
+    from its position: with 16-bit states two producer warps count them to place each unit's chunk fills."""
+    w = wl.Workload("padb", B=160, Hk=2, Hv=32, dk=64, dv=64, steps=2, state_dtype=sdt, in_dtype="bf16",
+                    num_slots=400, seed=7)
+    slots = wl.slots(w).copy()
+    slots[::3] = -1
+    slots[1::7] = w.num_slots + 5
+    err, *_ = _run_full(w, slots=slots)
+    assert err == gdn.DEVERR_SLOT
+
+
 def test_empty_batch():
     pool = torch.zeros((2, 2, 32, 32), device="cuda")
     z = torch.zeros(0, device="cuda")

@@ -81,6 +81,17 @@ def test_decode_padding_out_of_range_and_narrow_output():
     assert _decode_all(w, slots=slots, out_dtype="bf16") == gdn.DEVERR_SLOT
 
 
+def test_decode_padding_bf16_over_several_batches():
+    """48 x 128 = 6,144 units, so CTAs take a second batch; padding and out-of-range sequences shift each
+    unit's chunk fills, which the two producer warps of a 16-bit state count."""
+    w = wl.Workload("m2pb", B=48, Hk=2, Hv=128, dk=64, dv=64, steps=2, state_dtype="bf16", in_dtype="bf16",
+                    num_slots=120, seed=54)
+    slots = wl.slots(w).copy()
+    slots[::3] = -1
+    slots[1::7] = w.num_slots + 3
+    assert _decode_all(w, slots=slots) == gdn.DEVERR_SLOT
+
+
 class M2Harness:
     """A Mamba2 replay cache on the GPU next to one oracle head per (sequence, head) unit."""
 
