@@ -26,9 +26,11 @@ _lib = None
 
 
 def lib() -> C.CDLL:
+    """The oracle library: this package's build, or the one ORACLE_LIBRARY names (the planted-mistake
+    tests point it at altered copies)."""
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
+        _lib = C.CDLL(os.environ.get("ORACLE_LIBRARY") or build())
         P, I, I64, D = C.c_void_p, C.c_int, C.c_int64, C.c_double
         sig = {
             "orc_round": (D, [D, I]),

@@ -1,0 +1,114 @@
+"""Planted mistakes in the oracle, on the CPU.
+
+Each mutant is a copy of the oracle's C sources with one plausible slip -- a
+dropped term, a wrong sign, a swapped index or operand, an off-by-one bound --
+compiled into its own library. The pin tests then run against that library in
+a child process and must fail. The regression fixture is left out of those
+runs: it was written by the oracle itself, so only the pins, which rest on
+closed forms, brute force and library routines, count here. A mutant that
+passed would mark a part of the oracle that nothing independent checks.
+"""
+import importlib
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+oracle_build = importlib.import_module("oracle.build")  # the module (the package re-exports its build())
+
+PINS = ["test_oracle_pins.py", "test_oracle_spec_pins.py", "test_oracle_replay2_pins.py",
+        "test_oracle_prefill_pins.py", "test_oracle_mamba2_pins.py"]
+
+# (name, source file, text, replacement); the text occurs exactly once unless the name says "first"
+MUTANTS = [
+    # gating and normalisation
+    ("softplus_without_log1p", "gdn_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 20.0 ? x : exp(x)"),
+    ("sigmoid_sign", "gdn_oracle.c", "*beta = 1.0 / (1.0 + exp(-b));", "*beta = 1.0 / (1.0 + exp(b));"),
+    ("decay_without_inner_exp", "gdn_oracle.c", "*alpha = exp(-exp(A_log) * softplus(a + dt_bias));",
+     "*alpha = exp(-A_log * softplus(a + dt_bias));"),
+    ("l2norm_eps_outside_sqrt", "gdn_oracle.c", "1.0 / sqrt(ss + 1e-6)", "1.0 / (sqrt(ss) + 1e-6)"),
+    ("query_scale_dropped_first", "gdn_oracle.c", "orc_l2norm(dk, qr, 1.0 / sqrt((double)dk), qn);",
+     "orc_l2norm(dk, qr, 1.0, qn);"),
+    # the rule
+    ("prediction_without_decay", "gdn_oracle.c", "beta * kn[i] * (v[j] - alpha * u);",
+     "beta * kn[i] * (v[j] - u);"),
+    ("correction_sign", "gdn_oracle.c", "beta * kn[i] * (v[j] - alpha * u);",
+     "beta * kn[i] * (v[j] + alpha * u);"),
+    ("state_not_decayed", "gdn_oracle.c", "col[i] = alpha * col[i] + beta", "col[i] = col[i] + beta"),
+    ("readout_before_update_first", "gdn_oracle.c",
+     "rule_step(dk, dv, Sd, kn, vv, alpha, beta);\n    readout(dk, dv, Sd, qn, out);",
+     "readout(dk, dv, Sd, qn, out);\n    rule_step(dk, dv, Sd, kn, vv, alpha, beta);"),
+    ("key_head_modulo", "gdn_oracle.c",
+     "int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h / group;\n        double* o = out + u * dv;",
+     "int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h % Hk;\n        double* o = out + u * dv;"),
+    # storage formats
+    ("rounding_truncates", "gdn_oracle.c", "nearbyint(ax / quantum)", "trunc(ax / quantum)"),
+    ("no_gradual_underflow", "gdn_oracle.c", "if (e < emin) e = emin;", "if (e < emin) return copysign(0.0, x);"),
+    # ReplaySSM
+    ("fold_one_entry_early", "gdn_oracle.c",
+     "if (meta[0] + T > L) fold(dk, dv, S0, sdt, ek, ev, idt, ealpha, ebeta, meta);",
+     "if (meta[0] + T >= L) fold(dk, dv, S0, sdt, ek, ev, idt, ealpha, ebeta, meta);"),
+    ("window_output_one_token_behind", "gdn_oracle.c", "rebuild(dk, dv, S0, sdt, c + t + 1,",
+     "rebuild(dk, dv, S0, sdt, c + t,"),
+    ("rollback_drops_one_more", "gdn_oracle.c", "int r = T - 1 - accepted;", "int r = T - accepted;"),
+    ("fold_predicts_from_master", "gdn_oracle.c", "for (int i = 0; i < dk; ++i) u += cr[i] * kn[i];",
+     "for (int i = 0; i < dk; ++i) u += cm[i] * kn[i];"),
+    # speculative step and prefill
+    ("spec_copies_negated", "gdn_oracle.c",
+     "if (write[t])\n            for (int64_t i = 0; i < n; ++i) orc_store(S_out,",
+     "if (!write[t])\n            for (int64_t i = 0; i < n; ++i) orc_store(S_out,"),
+    ("prefill_write_back_off_by_one", "gdn_oracle.c", "if ((t + 1) % interval == 0 || t == T - 1)",
+     "if (t % interval == 0 || t == T - 1)"),
+    ("prefill_continues_unrounded", "gdn_oracle.c",
+     "for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);\n            load_vec(S, 0, (int)n, sdt, Sd);",
+     "for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);"),
+    # Mamba2
+    ("m2_skip_term_dropped", "mamba2_oracle.c", "y[p] = acc + D * x[p];", "y[p] = acc;"),
+    ("m2_step_size_dropped", "mamba2_oracle.c", "+ delta * x[p] * Bv[i];", "+ x[p] * Bv[i];"),
+    ("m2_group_modulo", "mamba2_oracle.c", "g = h / per_group;", "g = h % G;"),
+    ("m2_update_reads_C", "mamba2_oracle.c", "m2_update(N, P, Sd, bv, xv, alpha, delta);",
+     "m2_update(N, P, Sd, cv, xv, alpha, delta);"),
+    ("m2_decay_without_inner_exp", "mamba2_oracle.c", "*alpha = exp(-exp(A_log) * *delta);",
+     "*alpha = exp(-A_log * *delta);"),
+    ("m2_window_output_one_token_behind", "mamba2_oracle.c", "m2_rebuild(N, P, S0, sdt, c + t + 1,",
+     "m2_rebuild(N, P, S0, sdt, c + t,"),
+]
+
+
+def _mutate(tmp, name, src, text, repl) -> str:
+    """Copy the oracle sources into tmp, plant the slip (none when src is None), build the copy."""
+    for f in oracle_build.SOURCES + oracle_build.HEADERS:
+        shutil.copy(os.path.join(oracle_build.HERE, f), tmp)
+    if src is not None:
+        path = os.path.join(tmp, src)
+        with open(path) as fh:
+            code = fh.read()
+        count = code.count(text)
+        assert count == 1 or (name.endswith("_first") and count > 1), f"{name}: text found {count} times"
+        with open(path, "w") as fh:
+            fh.write(code.replace(text, repl, 1))
+    return oracle_build.build(force=True, src_dir=tmp, out=os.path.join(tmp, "lib", "liboracle.so"))
+
+
+def _run_pins(lib):
+    env = dict(os.environ, ORACLE_LIBRARY=lib)
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-k",
+                           "not regression_fixture", *[os.path.join(ROOT, "tests", p) for p in PINS]],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_unaltered_copy_passes_the_pins(tmp_path):
+    """The control: the same harness on an unaltered copy passes, so a failing mutant run means the slip."""
+    run = _run_pins(_mutate(str(tmp_path), "control", None, None, None))
+    assert run.returncode == 0, run.stdout[-3000:]
+
+
+@pytest.mark.parametrize("name,src,text,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, src, text, repl, tmp_path):
+    run = _run_pins(_mutate(str(tmp_path), name, src, text, repl))
+    assert run.returncode == 1, f"{name}: the pins did not fail (exit {run.returncode})\n{run.stdout[-3000:]}"
