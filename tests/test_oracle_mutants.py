@@ -46,7 +46,12 @@ MUTANTS = [
     ("key_head_modulo", "gdn_oracle.c",
      "int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h / group;\n        double* o = out + u * dv;",
      "int bi = (int)(u / Hv), h = (int)(u % Hv), kh = h % Hk;\n        double* o = out + u * dv;"),
+    ("key_gets_query_scale_first", "gdn_oracle.c", "orc_l2norm(dk, kr, 1.0, kn);",
+     "orc_l2norm(dk, kr, 1.0 / sqrt((double)dk), kn);"),
+    ("bad_count_of_padding_first", "gdn_oracle.c", "if (slot >= num_slots) bad += 1;", "if (slot < 0) bad += 1;"),
     # storage formats
+    ("bf16_load_shift", "gdn_oracle.c", "uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
+    ("f16_subnormal_scale", "gdn_oracle.c", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     ("rounding_truncates", "gdn_oracle.c", "nearbyint(ax / quantum)", "trunc(ax / quantum)"),
     ("no_gradual_underflow", "gdn_oracle.c", "if (e < emin) e = emin;", "if (e < emin) return copysign(0.0, x);"),
     # ReplaySSM
@@ -67,12 +72,27 @@ MUTANTS = [
     ("prefill_continues_unrounded", "gdn_oracle.c",
      "for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);\n            load_vec(S, 0, (int)n, sdt, Sd);",
      "for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);"),
+    ("flush_ignores_force", "gdn_oracle.c",
+     "if (force ? meta[0] > 0 : meta[0] == L) fold(dk, dv, S0, sdt,", "if (meta[0] == L) fold(dk, dv, S0, sdt,"),
+    ("rollback_past_checkpoint", "gdn_oracle.c", "if (meta[0] - r < 0) return -2;\n", ""),
+    ("gates_swapped_first", "gdn_oracle.c", "orc_load(a, u, idt), orc_load(b, u, idt)",
+     "orc_load(b, u, idt), orc_load(a, u, idt)"),
+    ("prefill_value_row_of_key_head", "gdn_oracle.c", "elem_ptr(v, (tok * Hv + h) * dv, idt)",
+     "elem_ptr(v, (tok * Hv + kh) * dv, idt)"),
+    ("prefill_gates_of_local_token", "gdn_oracle.c",
+     "orc_load(a, tok * Hv + h, idt), orc_load(b, tok * Hv + h, idt)",
+     "orc_load(a, t * Hv + h, idt), orc_load(b, t * Hv + h, idt)"),
     # Mamba2
+    ("m2_flush_ignores_force", "mamba2_oracle.c", "if (meta[0] == L || (force && meta[0] > 0)) m2_fold(",
+     "if (meta[0] == L) m2_fold("),
     ("m2_skip_term_dropped", "mamba2_oracle.c", "y[p] = acc + D * x[p];", "y[p] = acc;"),
     ("m2_step_size_dropped", "mamba2_oracle.c", "+ delta * x[p] * Bv[i];", "+ x[p] * Bv[i];"),
     ("m2_group_modulo", "mamba2_oracle.c", "g = h / per_group;", "g = h % G;"),
     ("m2_update_reads_C", "mamba2_oracle.c", "m2_update(N, P, Sd, bv, xv, alpha, delta);",
      "m2_update(N, P, Sd, cv, xv, alpha, delta);"),
+    ("m2_readout_before_update", "mamba2_oracle.c",
+     "m2_update(N, P, Sd, bv, xv, alpha, delta);\n    m2_readout(N, P, Sd, cv, xv, D, out);",
+     "m2_readout(N, P, Sd, cv, xv, D, out);\n    m2_update(N, P, Sd, bv, xv, alpha, delta);"),
     ("m2_decay_without_inner_exp", "mamba2_oracle.c", "*alpha = exp(-exp(A_log) * *delta);",
      "*alpha = exp(-A_log * *delta);"),
     ("m2_window_output_one_token_behind", "mamba2_oracle.c", "m2_rebuild(N, P, S0, sdt, c + t + 1,",

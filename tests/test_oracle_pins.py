@@ -251,15 +251,15 @@ def test_gqa_equals_mha_with_repeated_key_heads():
 
 
 def test_slots_padding_and_out_of_range():
-    B, Hk, Hv, dk, dv = 3, 1, 2, 4, 4
+    B, Hk, Hv, dk, dv = 4, 1, 2, 4, 4
     x = _batch(B, Hk, Hv, dk, dv, 10)
     pool = np.random.default_rng(11).standard_normal((2, Hv, dv, dk)).astype(np.float32)
     pool0 = pool.copy()
-    slots = np.array([-1, 2, 1], dtype=np.int32)
+    slots = np.array([-1, 2, 1, -3], dtype=np.int32)
     out, bad = oracle.decode_step(pool, "f32", slots, x["q"], x["k"], x["v"], x["a"], x["b"], "f64",
                                   np.zeros(Hv, np.float32), np.zeros(Hv, np.float32))
-    assert bad == Hv  # counted per (sequence, head) unit
-    assert np.all(out[0] == 0) and np.all(out[1] == 0) and np.any(out[2] != 0)
+    assert bad == Hv  # the out-of-range sequence, counted per (sequence, head) unit; padding is not an error
+    assert np.all(out[0] == 0) and np.all(out[1] == 0) and np.any(out[2] != 0) and np.all(out[3] == 0)
     assert np.array_equal(pool[0], pool0[0]) and not np.array_equal(pool[1], pool0[1])
 
 
@@ -423,6 +423,10 @@ def test_fold_rule_and_pointer_bookkeeping():
     assert (h.count, h.ckpt_pos) == (0, 18)
     with pytest.raises(ValueError):
         h.rollback(4, 4)  # accepted must be < T
+    h.window(**one, A_log=0.0, dt_bias=0.0)
+    with pytest.raises(ValueError):
+        h.rollback(3, 0)  # two tokens back would pass the checkpoint, whose entries are folded away
+    assert (h.count, h.pos, h.ckpt_pos) == (1, 19, 18)
     with pytest.raises(ValueError):
         h.window(**_tokens(1, dk, dv, 28, T=5)[0], A_log=0.0, dt_bias=0.0)  # T > L
 
