@@ -82,6 +82,13 @@ MUTANTS = [
     ("prefill_gates_of_local_token", "gdn_oracle.c",
      "orc_load(a, tok * Hv + h, idt), orc_load(b, tok * Hv + h, idt)",
      "orc_load(a, t * Hv + h, idt), orc_load(b, t * Hv + h, idt)"),
+    ("prefill_outputs_at_sequence_local_rows", "gdn_oracle.c",
+     "for (int j = 0; j < dv; ++j) out[((int64_t)(t0 + t) * Hv + h) * dv + j] = o[(int64_t)t * dv + j];",
+     "for (int j = 0; j < dv; ++j) out[((int64_t)t * Hv + h) * dv + j] = o[(int64_t)t * dv + j];"),
+    ("spec_copies_to_first_destination", "gdn_oracle.c",
+     "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T + t] * Hv + h) * n * esz,",
+     "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T] * Hv + h) * n * esz,"),
+    ("read_copy_rounds_unrounded_master", "gdn_oracle.c", "orc_store(Rd, i, rdt, m);", "orc_store(Rd, i, rdt, Sm[i]);"),
     # Mamba2
     ("m2_flush_ignores_force", "mamba2_oracle.c", "if (meta[0] == L || (force && meta[0] > 0)) m2_fold(",
      "if (meta[0] == L) m2_fold("),

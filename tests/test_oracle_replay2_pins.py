@@ -6,7 +6,8 @@ low-precision copy for reading. Fixed independently of the mode's code:
   folds, verify windows and rollbacks;
 - between folds its outputs are those of a single-checkpoint replay whose
   checkpoint is the current read copy;
-- after a fold the read copy is the stored master rounded to the read dtype;
+- after a fold the read copy is the stored master rounded to the read dtype (a value just above a
+  bf16 tie shows the fp32 store comes first);
 - dk = dv = 1: the fold's closed form, whose prediction comes from the read copy
   (a fold that predicted from the master gives a different value);
 - beta = 0: the fold is the pure decay of the master.
@@ -118,3 +119,19 @@ def test_pure_decay_fold():
         two.window(q, k, v, np.array([-dt_bias]), np.array([-np.inf]), A_log, dt_bias)
     assert np.allclose(two.S0, 0.5 ** L * M0, rtol=1e-14, atol=0)
     assert np.array_equal(two.Sr, oracle.round_to(two.S0, "bf16"))
+
+
+def test_copy_is_the_stored_master_rounded_once_more():
+    """The copy is the stored fp32 master rounded to bf16, not the fold's fp64 value rounded to bf16.
+    With dk = dv = 1, alpha = 1 (a = -inf), beta = 1/2 (b = 0) and a zero checkpoint, one buffered
+    token folds to 1 + 2^-8 + 2^-30, just above the bf16 tie between 1 and 1 + 2^-7. The master stores
+    the fp32 tie 1 + 2^-8 itself, which rounds to even: the copy is 1. Rounding the fold value directly
+    would give 1 + 2^-7."""
+    h = oracle.ReplayHead(np.zeros((1, 1)), "f32", "f64", 1, read_dtype="bf16")
+    kn = 1.0 / math.sqrt(1.0 + EPS)  # the normalised key of k = 1
+    target = 1.0 + 2.0 ** -8 + 2.0 ** -30
+    one, a, b = np.ones((1, 1)), np.array([-np.inf]), np.array([0.0])
+    h.window(one, one, np.array([[target / (0.5 * kn)]]), a, b, A_log=0.0, dt_bias=0.0)
+    h.window(one, one, np.zeros((1, 1)), a, b, A_log=0.0, dt_bias=0.0)  # 1 + 1 > L: the fold comes first
+    assert float(h.S0[0, 0]) == 1.0 + 2.0 ** -8
+    assert float(oracle.load(h.Sr, "bf16")[0, 0]) == 1.0
