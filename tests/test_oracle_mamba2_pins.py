@@ -31,6 +31,10 @@ def test_gating_closed_forms():
     assert de == pytest.approx(math.log(2), rel=1e-15) and al == pytest.approx(0.5, rel=1e-15)
     al, de = oracle.m2_gating(math.log(3.0), 0.25, -0.25)  # A = -3, delta = ln 2: alpha = 2^-3
     assert al == pytest.approx(0.125, rel=1e-14)
+    al, de = oracle.m2_gating(0.0, 0.0, math.log(15.0))  # below the cut-over: delta = ln 16, alpha = 1/16
+    assert de == pytest.approx(4 * math.log(2), rel=1e-14) and al == pytest.approx(1 / 16, rel=1e-14)
+    al, de = oracle.m2_gating(0.0, 0.0, math.log(2.0 ** 26 - 1))  # still below it: delta = 26 ln 2
+    assert al == pytest.approx(2.0 ** -26, rel=1e-12)
     al, de = oracle.m2_gating(0.0, 10.0, 20.5)  # above the cut-over softplus is the identity
     assert de == 30.5 and al == pytest.approx(math.exp(-30.5), rel=1e-14)
     al, de = oracle.m2_gating(1.0, 0.0, -800.0)

@@ -13,8 +13,7 @@ import os
 import shutil
 import subprocess
 import sys
-
-import pytest
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -89,7 +88,25 @@ MUTANTS = [
      "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T + t] * Hv + h) * n * esz,",
      "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T] * Hv + h) * n * esz,"),
     ("read_copy_rounds_unrounded_master", "gdn_oracle.c", "orc_store(Rd, i, rdt, m);", "orc_store(Rd, i, rdt, Sm[i]);"),
+    ("spec_continues_from_rounded_copy", "gdn_oracle.c",
+     "for (int64_t i = 0; i < n; ++i) orc_store(S_out, (int64_t)t * n + i, sdt, Sd[i]);",
+     "for (int64_t i = 0; i < n; ++i) orc_store(S_out, (int64_t)t * n + i, sdt, Sd[i]);\n"
+     "        if (write[t]) load_vec(S_out, (int64_t)t * n, (int)n, sdt, Sd);"),
+    ("decode_reads_out_the_rounded_state", "gdn_oracle.c",
+     "    readout(dk, dv, Sd, qn, out);\n    for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);",
+     "    for (int64_t i = 0; i < n; ++i) orc_store(S, i, sdt, Sd[i]);\n"
+     "    load_vec(S, 0, (int)n, sdt, Sd);\n    readout(dk, dv, Sd, qn, out);"),
+    ("prefill_final_state_not_stored", "gdn_oracle.c", "if ((t + 1) % interval == 0 || t == T - 1)",
+     "if ((t + 1) % interval == 0)"),
+    ("window_gates_in_one_entry", "gdn_oracle.c",
+     "orc_gating(A_log, dt_bias, a[t], b[t], &ealpha[c + t], &ebeta[c + t]);",
+     "orc_gating(A_log, dt_bias, a[t], b[t], &ealpha[c], &ebeta[c]);"),
+    ("dt_bias_outside_softplus", "gdn_oracle.c", "*alpha = exp(-exp(A_log) * softplus(a + dt_bias));",
+     "*alpha = exp(-exp(A_log) * (softplus(a) + dt_bias));"),
+    ("softplus_cut_over_at_2", "gdn_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 2.0 ? x : log1p(exp(x))"),
     # Mamba2
+    ("m2_softplus_cut_over_at_2", "mamba2_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 2.0 ? x : log1p(exp(x))"),
+    ("m2_dt_bias_dropped", "mamba2_oracle.c", "*delta = softplus_m2(dt + dt_bias);", "*delta = softplus_m2(dt);"),
     ("m2_flush_ignores_force", "mamba2_oracle.c", "if (meta[0] == L || (force && meta[0] > 0)) m2_fold(",
      "if (meta[0] == L) m2_fold("),
     ("m2_skip_term_dropped", "mamba2_oracle.c", "y[p] = acc + D * x[p];", "y[p] = acc;"),
@@ -135,7 +152,18 @@ def test_unaltered_copy_passes_the_pins(tmp_path):
     assert run.returncode == 0, run.stdout[-3000:]
 
 
-@pytest.mark.parametrize("name,src,text,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(name, src, text, repl, tmp_path):
-    run = _run_pins(_mutate(str(tmp_path), name, src, text, repl))
-    assert run.returncode == 1, f"{name}: the pins did not fail (exit {run.returncode})\n{run.stdout[-3000:]}"
+def test_pins_catch_every_planted_mistake(tmp_path):
+    """Every mutant, built and checked in parallel (each in its own directory and child process)."""
+
+    def check(i):
+        name, src, text, repl = MUTANTS[i]
+        d = tmp_path / f"m{i}"
+        d.mkdir()
+        run = _run_pins(_mutate(str(d), name, src, text, repl))
+        return name, run.returncode, run.stdout[-1500:]
+
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(check, range(len(MUTANTS))))
+    survivors = [(name, code, out) for name, code, out in results if code != 1]
+    assert not survivors, "mutants the pins did not catch:\n" + "\n".join(
+        f"{name} (exit {code})\n{out}" for name, code, out in survivors)

@@ -93,6 +93,9 @@ def test_gating_closed_forms():
     assert oracle.gating(0.0, 0.0, 0.0, -math.inf)[1] == 0.0
     assert oracle.gating(0.0, 0.0, math.inf, 0.0)[0] == 0.0
     assert oracle.gating(-math.inf, 0.3, 1.7, 0.0)[0] == 1.0
+    # below the cut-over softplus is ln(1 + e^x), however large x: ln 15 -> ln 16, ln(2^26 - 1) -> 26 ln 2
+    assert oracle.gating(0.0, 0.0, math.log(15.0), 0.0)[0] == pytest.approx(1 / 16, rel=1e-14)
+    assert oracle.gating(0.0, 0.0, math.log(2.0 ** 26 - 1), 0.0)[0] == pytest.approx(2.0 ** -26, rel=1e-12)
     # above the softplus cut-over the argument passes through: exp(A_log)=1/25, x=25 -> e^-1
     al, _ = oracle.gating(math.log(1 / 25), 5.0, 20.0, 0.0)
     assert al == pytest.approx(math.exp(-1.0), rel=1e-14)
