@@ -104,6 +104,16 @@ MUTANTS = [
     ("dt_bias_outside_softplus", "gdn_oracle.c", "*alpha = exp(-exp(A_log) * softplus(a + dt_bias));",
      "*alpha = exp(-exp(A_log) * (softplus(a) + dt_bias));"),
     ("softplus_cut_over_at_2", "gdn_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 2.0 ? x : log1p(exp(x))"),
+    ("l1_norm_for_l2", "gdn_oracle.c", "ss += x[i] * x[i];", "ss += fabs(x[i]);"),
+    ("no_overflow_to_inf", "gdn_oracle.c", "if (r > maxfin) r = INFINITY;", ""),
+    ("decode_state_at_key_head_stride_first", "gdn_oracle.c",
+     "void* S = (char*)pool + ((int64_t)slot * Hv + h) * (int64_t)dv * dk * orc_dtype_size(sdt);",
+     "void* S = (char*)pool + ((int64_t)slot * Hk + h) * (int64_t)dv * dk * orc_dtype_size(sdt);"),
+    ("replay_query_unscaled", "gdn_oracle.c", "orc_l2norm(dk, qv, 1.0 / sqrt((double)dk), qv + dk);",
+     "orc_l2norm(dk, qv, 1.0, qv + dk);"),
+    ("replay_keys_unnormalised", "gdn_oracle.c", "rule_step(dk, dv, S, kn, vv, ea[e], eb[e]);",
+     "rule_step(dk, dv, S, kr, vv, ea[e], eb[e]);"),
+    ("fold_master_decays_the_copy", "gdn_oracle.c", "cm[i] = ea[e] * cm[i] + eb[e]", "cm[i] = ea[e] * cr[i] + eb[e]"),
     # Mamba2
     ("m2_softplus_cut_over_at_2", "mamba2_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 2.0 ? x : log1p(exp(x))"),
     ("m2_dt_bias_dropped", "mamba2_oracle.c", "*delta = softplus_m2(dt + dt_bias);", "*delta = softplus_m2(dt);"),
