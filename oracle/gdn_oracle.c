@@ -473,44 +473,25 @@ int orc_replay_window(int dk, int dv, int L, void* S0, int sdt, void* ek, void* 
 /* ------------------------------------------------------------------ ReplaySSM, two checkpoints */
 
 /* A high-precision checkpoint M for the recurrence and a low-precision copy Rd
- * for reading. Folding: every buffered entry's update is taken from the state
- * rebuilt from the read copy -- the prediction S^T k, and with it the
- * correction, come from the copy that every output reads -- and the same
- * update is applied to the master. Then M is rounded to mdt and Rd is
- * rewritten as the rounded master, rounded to rdt. With Rd holding the same
- * values as M this is the single-checkpoint fold. */
+ * for reading (AREX ReplaySSM article, section "缓存输入而非状态", its
+ * paragraph on precision: the recurrence runs on the high-precision
+ * checkpoint, reads go to the low-precision copy). Folding re-runs every
+ * buffered entry's raw inputs (k, v, alpha, beta) through the rule starting
+ * from M -- each prediction S^T k comes from the master's own state -- rounds
+ * the result to mdt and stores it; then Rd is rewritten as that stored master
+ * rounded to rdt. The read copy plays no part in a fold: the master evolves as
+ * a single-checkpoint replay in mdt would. */
 static void fold2(int dk, int dv, void* M, int mdt, void* Rd, int rdt, const void* ek, const void* ev, int idt,
                   const double* ea, const double* eb, int32_t* meta) {
     int64_t n = (int64_t)dk * dv;
-    double* Sr = (double*)malloc(sizeof(double) * (size_t)n);
     double* Sm = (double*)malloc(sizeof(double) * (size_t)n);
-    double* tmp = (double*)malloc(sizeof(double) * (size_t)(2 * dk + dv));
-    double *kr = tmp, *kn = tmp + dk, *vv = tmp + 2 * dk;
-    load_vec(Rd, 0, (int)n, rdt, Sr);
-    load_vec(M, 0, (int)n, mdt, Sm);
-    for (int e = 0; e < meta[0]; ++e) {
-        load_vec(ek, (int64_t)e * dk, dk, idt, kr);
-        load_vec(ev, (int64_t)e * dv, dv, idt, vv);
-        orc_l2norm(dk, kr, 1.0, kn);
-        for (int j = 0; j < dv; ++j) {
-            double* cr = Sr + (int64_t)j * dk;
-            double* cm = Sm + (int64_t)j * dk;
-            double u = 0.0;
-            for (int i = 0; i < dk; ++i) u += cr[i] * kn[i];
-            for (int i = 0; i < dk; ++i) {
-                cr[i] = ea[e] * cr[i] + eb[e] * kn[i] * (vv[j] - ea[e] * u);
-                cm[i] = ea[e] * cm[i] + eb[e] * kn[i] * (vv[j] - ea[e] * u);
-            }
-        }
-    }
+    rebuild(dk, dv, M, mdt, meta[0], ek, ev, idt, ea, eb, Sm);
     for (int64_t i = 0; i < n; ++i) {
         double m = orc_round(Sm[i], mdt);
         orc_store(M, i, mdt, m);
         orc_store(Rd, i, rdt, m);
     }
-    free(tmp);
     free(Sm);
-    free(Sr);
     meta[0] = 0;
     meta[2] = meta[1];
 }

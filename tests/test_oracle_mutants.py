@@ -60,8 +60,8 @@ MUTANTS = [
     ("window_output_one_token_behind", "gdn_oracle.c", "rebuild(dk, dv, S0, sdt, c + t + 1,",
      "rebuild(dk, dv, S0, sdt, c + t,"),
     ("rollback_drops_one_more", "gdn_oracle.c", "int r = T - 1 - accepted;", "int r = T - accepted;"),
-    ("fold_predicts_from_master", "gdn_oracle.c", "for (int i = 0; i < dk; ++i) u += cr[i] * kn[i];",
-     "for (int i = 0; i < dk; ++i) u += cm[i] * kn[i];"),
+    ("fold_runs_from_the_read_copy", "gdn_oracle.c", "rebuild(dk, dv, M, mdt, meta[0],",
+     "rebuild(dk, dv, Rd, rdt, meta[0],"),
     # speculative step and prefill
     ("spec_copies_negated", "gdn_oracle.c",
      "if (write[t])\n            for (int64_t i = 0; i < n; ++i) orc_store(S_out,",
@@ -88,6 +88,7 @@ MUTANTS = [
      "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T + t] * Hv + h) * n * esz,",
      "memcpy((char*)pool + ((int64_t)dst_slots[(int64_t)bi * T] * Hv + h) * n * esz,"),
     ("read_copy_rounds_unrounded_master", "gdn_oracle.c", "orc_store(Rd, i, rdt, m);", "orc_store(Rd, i, rdt, Sm[i]);"),
+    ("fold2_master_not_stored", "gdn_oracle.c", "orc_store(M, i, mdt, m);", ""),
     ("spec_continues_from_rounded_copy", "gdn_oracle.c",
      "for (int64_t i = 0; i < n; ++i) orc_store(S_out, (int64_t)t * n + i, sdt, Sd[i]);",
      "for (int64_t i = 0; i < n; ++i) orc_store(S_out, (int64_t)t * n + i, sdt, Sd[i]);\n"
@@ -113,7 +114,6 @@ MUTANTS = [
      "orc_l2norm(dk, qv, 1.0, qv + dk);"),
     ("replay_keys_unnormalised", "gdn_oracle.c", "rule_step(dk, dv, S, kn, vv, ea[e], eb[e]);",
      "rule_step(dk, dv, S, kr, vv, ea[e], eb[e]);"),
-    ("fold_master_decays_the_copy", "gdn_oracle.c", "cm[i] = ea[e] * cm[i] + eb[e]", "cm[i] = ea[e] * cr[i] + eb[e]"),
     # Mamba2
     ("m2_softplus_cut_over_at_2", "mamba2_oracle.c", "x > 20.0 ? x : log1p(exp(x))", "x > 2.0 ? x : log1p(exp(x))"),
     ("m2_dt_bias_dropped", "mamba2_oracle.c", "*delta = softplus_m2(dt + dt_bias);", "*delta = softplus_m2(dt);"),

@@ -8,8 +8,13 @@ low-precision copy for reading. Fixed independently of the mode's code:
   checkpoint is the current read copy;
 - after a fold the read copy is the stored master rounded to the read dtype (a value just above a
   bf16 tie shows the fp32 store comes first);
-- dk = dv = 1: the fold's closed form, whose prediction comes from the read copy
-  (a fold that predicted from the master gives a different value);
+- dk = dv = 1: the fold's closed form, whose prediction comes from the master
+  (the AREX ReplaySSM article, section "缓存输入而非状态", precision paragraph:
+  the recurrence runs on the high-precision checkpoint); a fold that predicted
+  from the read copy gives a different value;
+- the master after any sequence of steps, windows, rollbacks and flushes is
+  the checkpoint of a single-checkpoint replay in the master's dtype fed the
+  same calls: the read copy never enters the recurrence;
 - beta = 0: the fold is the pure decay of the master.
 """
 import math
@@ -82,9 +87,9 @@ def test_outputs_read_the_copy_and_folds_refresh_it(mdt, rdt):
     assert folds >= 4
 
 
-def test_scalar_fold_predicts_from_the_read_copy():
+def test_scalar_fold_predicts_from_the_master():
     """dk = dv = 1 with one buffered entry: the fold gives m' = alpha m + k w with
-    w = beta (v - alpha r k), r the read copy, k = x / sqrt(x^2 + eps)."""
+    w = beta (v - alpha m k), m the master, k = x / sqrt(x^2 + eps)."""
     m = 0.7372654321  # not a bf16 value, so the read copy differs from the master
     two = oracle.ReplayHead(np.array([[m]]), "f64", "f64", 1, read_dtype="bf16")
     r_ = float(oracle.load(two.Sr, "bf16")[0, 0])
@@ -98,13 +103,43 @@ def test_scalar_fold_predicts_from_the_read_copy():
     two.window(np.array([[0.5]]), np.array([[x]]), np.array([[v]]), np.array([a_in]), np.array([b_in]), A_log,
                dt_bias)
     kn = x / math.sqrt(x * x + EPS)
-    w = beta * (v - alpha * r_ * kn)
-    expect = alpha * m + kn * w
+    expect = alpha * m + kn * beta * (v - alpha * m * kn)
     assert two.S0[0, 0] == pytest.approx(expect, rel=1e-15)
-    wrong = alpha * m + kn * beta * (v - alpha * m * kn)  # a prediction from the master instead
+    wrong = alpha * m + kn * beta * (v - alpha * r_ * kn)  # a prediction from the read copy instead
     assert abs(two.S0[0, 0] - wrong) > 1e-6
     assert float(oracle.load(two.Sr, "bf16")[0, 0]) == float(oracle.load(oracle.round_to(np.array([expect]), "bf16"),
                                                                           "bf16")[0])
+
+
+@pytest.mark.parametrize("mdt,rdt", [("f32", "bf16"), ("f32", "f16")])
+def test_master_is_the_single_checkpoint_replay_in_its_dtype(mdt, rdt):
+    """The read copy never enters the recurrence: after every call the master equals the checkpoint
+    of a single-checkpoint replay stored in the master's dtype and fed the same calls (steps, T = 3
+    windows with rollbacks, forced flushes), bit for bit, although the outputs differ."""
+    dk, dv, L = 12, 10, 5
+    r = np.random.default_rng(11)
+    S0 = oracle.round_to(0.3 * r.standard_normal((dv, dk)), mdt)
+    two = oracle.ReplayHead(S0, mdt, "f32", L, read_dtype=rdt)
+    one = oracle.ReplayHead(S0, mdt, "f32", L)
+    differ = False
+    folds = 0
+    for s in range(40):
+        T = 3 if s % 5 == 4 else 1
+        q, k, v, a, b = (x.astype(np.float32) for x in _tokens(r, T, dk, dv))
+        a, b = a.astype(np.float64), b.astype(np.float64)
+        folds += two.count + T > L
+        o2 = two.window(q, k, v, a, b, 0.3, 0.1)
+        o1 = one.window(q, k, v, a, b, 0.3, 0.1)
+        differ = differ or not np.array_equal(o2, o1)
+        if T > 1:
+            acc = int(r.integers(0, T))
+            two.rollback(T, acc), one.rollback(T, acc)
+        if s % 13 == 12:
+            two.flush(True), one.flush(True)
+            folds += 1
+        assert np.array_equal(two.S0, one.S0), s
+        assert (two.count, two.ckpt_pos) == (one.count, one.ckpt_pos)
+    assert differ and folds >= 6
 
 
 def test_pure_decay_fold():
