@@ -92,7 +92,7 @@ int replay_common(const char* fn, int rule, const gdn_dims* dims, const gdn_repl
         return fail(GDN_ERR_NULL, "%s: a cache, slots or dev_err pointer is NULL", fn);
     if (!dtype_ok(c->ckpt_dtype) || !dtype_ok(c->ring_dtype))
         return fail(GDN_ERR_DTYPE, "%s: unsupported cache dtype (ckpt=%d ring=%d)", fn, c->ckpt_dtype, c->ring_dtype);
-    if (c->L < 1 || c->L > gdn::L_MAX) return fail(GDN_ERR_WINDOW, "%s: L=%d not in [1, 32]", fn, c->L);
+    if (c->L < 1 || c->L > gdn::L_MAX) return fail(GDN_ERR_WINDOW, "%s: L=%d not in [1, 64]", fn, c->L);
     if (dims->dv % 32 != 0) return fail(GDN_ERR_SHAPE, "%s: dv=%d must be a multiple of 32", fn, dims->dv);
     if (T > 0) {
         if (T > c->L || T > gdn::WINDOW_MAX)
@@ -294,12 +294,16 @@ int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int3
     if (rc) return rc;
     if (!cache) return fail(GDN_ERR_NULL, "%s: cache is NULL", fn);
     if (dims->B == 0) return GDN_OK;
-    if (!cache->pos || !cache->ckpt_pos || !slots || !accepted || !dev_err)
-        return fail(GDN_ERR_NULL, "%s: pos, ckpt_pos, slots, accepted or dev_err is NULL", fn);
+    if (!cache->pos || !cache->ckpt_pos || !cache->ring_rec || !slots || !accepted || !dev_err)
+        return fail(GDN_ERR_NULL, "%s: pos, ckpt_pos, ring_rec, slots, accepted or dev_err is NULL", fn);
+    if (cache->L < 1 || cache->L > gdn::L_MAX) return fail(GDN_ERR_WINDOW, "%s: L=%d not in [1, 64]", fn, cache->L);
     if (T < 1 || T > cache->L || T > gdn::WINDOW_MAX)
         return fail(GDN_ERR_WINDOW, "%s: T=%d not in [1, min(L, 8)]", fn, T);
-    return launched(gdn::launch_rollback(cache->pos, cache->ckpt_pos, slots, accepted, dims->B, dims->Hv, T,
-                                         dims->num_slots, dev_err, static_cast<cudaStream_t>(stream)),
+    if (!aligned_to(cache->pos, 4) || !aligned_to(cache->ckpt_pos, 4) || !aligned16(cache->ring_rec))
+        return fail(GDN_ERR_ALIGN, "%s: pos, ckpt_pos or ring_rec misaligned", fn);
+    return launched(gdn::launch_rollback(cache->pos, cache->ckpt_pos, cache->ring_rec, slots, accepted, dims->B,
+                                         dims->Hv, T, cache->L, dims->dv, dims->num_slots, dev_err,
+                                         static_cast<cudaStream_t>(stream)),
                     fn);
 }
 

@@ -37,7 +37,9 @@ cudaError_t dispatch_spec_f16(int dk, int tmax, SpecArgs& a, cudaStream_t stream
 // Prefill with a rounded write-back per chunk.
 cudaError_t dispatch_prefill(int state_dtype, int dk, PrefillArgs& a, cudaStream_t stream);
 
-cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, const int32_t* slots, const int32_t* accepted,
-                            int B, int Hv, int T, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
+// Rollback: pointer moves, checked against the window-length marker in each window's first record.
+cudaError_t launch_rollback(int32_t* pos, const int32_t* ckpt_pos, float* ring_rec, const int32_t* slots,
+                            const int32_t* accepted, int B, int Hv, int T, int L, int dv, int64_t num_slots,
+                            int32_t* dev_err, cudaStream_t stream);
 
 }  // namespace gdn

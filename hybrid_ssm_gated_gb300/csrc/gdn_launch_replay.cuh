@@ -32,7 +32,7 @@ constexpr int replay_warps() {
 #define GDN_REPLAY_MIN_CHUNKS 8
 #endif
 
-// Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype, nchunk, mnchunk).
+// Fill the shared-memory layout fields of `a` (needs T, L, dv, in_dtype, nchunk, mnchunk, ckpt_copy).
 // Returns the total dynamic shared memory in bytes, or -1 if it cannot fit. The chunk ring holds at
 // least one whole unit: a unit's head barrier completes only once every chunk of the unit is armed,
 // so a unit with more chunks than stages could never complete.
@@ -41,13 +41,15 @@ int replay_layout(ReplayArgs& a, int smem_limit, int sums_bytes) {
     const int need = a.nchunk > a.mnchunk ? a.nchunk : a.mnchunk;
     const int in_sz = dtype_size(a.in_dtype);
     const int T = a.T, L = a.L;
-    // head stage: meta | window q, k, v rows | ring keys | ring records | coefficient table
+    // head stage: meta | window q, k, v rows | ring keys | ring records | ring values (two-checkpoint
+    // folds only) | coefficient table
     a.off_wq = REPLAY_META;
     a.off_wk = a.off_wq + T * DK * in_sz;
     a.off_wv = a.off_wk + T * DK * in_sz;
     a.off_rk = align_up(a.off_wv + T * a.dv * in_sz, 16);
     a.off_rec = a.off_rk + L * DK * in_sz;
-    a.off_coef = a.off_rec + L * (4 + a.dv) * 4;
+    a.off_rv = a.off_rec + L * (4 + a.dv) * 4;
+    a.off_coef = a.off_rv + (a.ckpt_copy ? L * a.dv * in_sz : 0);
     a.head_bytes = align_up(a.off_coef + (L + TMAX) * 2 * TMAX * 4, 128);
     auto total = [&](int ns, int nh) {
         // mbarriers: 2 per chunk stage, 3 per head stage; a 4-byte counter per head stage

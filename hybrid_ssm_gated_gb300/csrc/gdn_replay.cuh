@@ -79,7 +79,7 @@
 
 namespace gdn {
 
-constexpr int L_MAX = 32;
+constexpr int L_MAX = 64;
 constexpr int WINDOW_MAX = 8;
 
 struct ReplayArgs {
@@ -112,7 +112,7 @@ struct ReplayArgs {
     int nstage, nhead;  // chunk and head ring depths
     float q_scale;
     // shared-memory layout, bytes
-    int head_bytes, off_wq, off_wk, off_wv, off_rk, off_rec, off_coef;  // inside a head stage
+    int head_bytes, off_wq, off_wk, off_wv, off_rk, off_rec, off_rv, off_coef;  // inside a head stage
     int heads_off, sums_off, bars_off;                                  // inside the CTA's buffer
 };
 
@@ -304,11 +304,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // The head barrier takes two arrivals: the first arms its copies; the second comes
                 // with the metadata once every S0 chunk of the unit is armed, so a consumer that has
                 // seen the head complete may wait on the unit's chunk barriers directly.
+                // a two-checkpoint fold also takes the buffered raw values: it re-runs the entries on the master
+                const bool fm = MIXED && f_i;
                 if (lane == 0) {
                     if (n >= NH) ok = mbar_wait(&hempty[hs], hph ^ 1);
                     if (ok) {
                         if (s_i >= 0)
-                            mbar_arrive_expect_tx(&hfull[hs], T * (2 * qbytes + vbytes) + c_i * (qbytes + recbytes));
+                            mbar_arrive_expect_tx(&hfull[hs], T * (2 * qbytes + vbytes) +
+                                                                  c_i * (qbytes + recbytes + (fm ? vbytes : 0u)));
                         else
                             mbar_arrive(&hfull[hs]);
                         ++nh;
@@ -333,13 +336,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
                 const int64_t unit_ring = ((int64_t)s_i * p.Hv + h) * L;
                 // a fold unit streams the master checkpoint, any other the one steps read
-                const bool fm = MIXED && f_i;
                 const int nck = fm ? p.mnchunk : p.nchunk;
                 const uint32_t ub = fm ? p.mrows * MROW_BYTES : cbytes;
                 const char* s0 = static_cast<const char*>(MIXED && !f_i ? p.ckpt_copy : p.ckpt) +
                                  ((int64_t)s_i * p.Hv + h) * p.dv * (fm ? MROW_BYTES : C::ROW_BYTES);
-                // Copies: lanes 0..3T-1 the window's q/k/v rows, the next four up to two ring ranges (keys,
-                // records), the others S0 chunks, at most NS of them at a time so that no lane waits for a
+                // Copies: lanes 0..3T-1 the window's q/k/v rows, the next four (six) up to two ring ranges
+                // (keys, records, and values for a two-checkpoint fold), the others S0 chunks, at most NS of them at a time so that no lane waits for a
                 // stage another lane is about to fill. A unit of more than two chunks issues its rows and
                 // ring first, then each chunk as soon as its stage is free: waiting for all of them would
                 // hold the rows back by up to a unit's worth of consumption (T = 4 windows over fp32
@@ -348,7 +350,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // only when the chunks do not fit). The split is compiled only where it can pay: in the
                 // single-token kernels of small units, even untaken, it cost up to 17%.
                 constexpr bool SPLIT = TMAX > 1 || (RULE == RULE_GDN && std::is_same<ST, float>::value && !MIXED);
-                const int hj = 3 * T + 4;
+                constexpr int NJ = MIXED ? 6 : 4;  // ring-range copy jobs
+                const int hj = 3 * T + NJ;
                 bool split = false;
                 if constexpr (SPLIT) split = nck > 2;
                 for (int c0 = 0, round = 0; ok && (round == 0 || c0 < nck); ++round) {
@@ -371,17 +374,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         bytes = kind == 2 ? vbytes : qbytes;
                         pol = pol_once;
                     } else if (round == 0 && lane < hj) {
-                        const int job = lane - 3 * T;  // 0/1: first ring range (keys, records); 2/3: wrapped range
-                        const int first = job < 2 ? 0 : n1, cnt = job < 2 ? n1 : c_i - n1, ridx = job < 2 ? rbase : 0;
+                        // job bit 0: the first ring range or the wrapped one; job / 2: keys, records, values
+                        const int job = lane - 3 * T, wrap = job & 1, kind = job >> 1;
+                        const int first = wrap ? n1 : 0, cnt = wrap ? c_i - n1 : n1, ridx = wrap ? 0 : rbase;
                         if (cnt > 0) {
-                            if ((job & 1) == 0) {
+                            if (kind == 0) {
                                 src = static_cast<const char*>(p.ring_k) + (unit_ring + ridx) * qbytes;
                                 dst = head + p.off_rk + first * qbytes;
                                 bytes = cnt * qbytes;
-                            } else {
+                            } else if (kind == 1) {
                                 src = reinterpret_cast<const char*>(p.ring_rec + (unit_ring + ridx) * rec_floats);
                                 dst = head + p.off_rec + first * recbytes;
                                 bytes = cnt * recbytes;
+                            } else if (fm) {
+                                src = static_cast<const char*>(p.ring_v) + (unit_ring + ridx) * vbytes;
+                                dst = head + p.off_rv + first * vbytes;
+                                bytes = cnt * vbytes;
                             }
                         }
                     }
@@ -530,16 +538,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 for (int e = 0; e < C::E / 2; ++e)
                     kw2[t][e] = make_float2(xk[2 * e], xk[2 * e + 1]), qw2[t][e] = make_float2(xq[2 * e], xq[2 * e + 1]);
             }
-            // decays of the ring entries, one lane per entry: R(f) = prod_{f<g<count} alpha_g by a suffix scan
+            // decays of the ring entries, lane f holding entries f and 32 + f:
+            // R(f) = prod_{f<g<count} alpha_g by suffix scans (the upper half only when L > 32)
             float suf = lane < count ? rec[lane * rec_floats] : 1.f;
+            float suf_hi = 1.f;
+            const bool ring_hi = L > 32;
+            if (ring_hi && lane + 32 < count) suf_hi = rec[(lane + 32) * rec_floats];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float o = __shfl_down_sync(FULL_MASK, suf, off);
                 if (lane + off < 32) suf *= o;
+                if (ring_hi) {
+                    const float oh = __shfl_down_sync(FULL_MASK, suf_hi, off);
+                    if (lane + off < 32) suf_hi *= oh;
+                }
             }
+            const float ghi = ring_hi ? __shfl_sync(FULL_MASK, suf_hi, 0) : 1.f;  // product of entries 32..count-1
+            suf *= ghi;
             const float gring = __shfl_sync(FULL_MASK, suf, 0);  // product of all ring alphas
             float R = __shfl_down_sync(FULL_MASK, suf, 1);
-            if (lane == 31) R = 1.f;
+            float R_hi = ring_hi ? __shfl_down_sync(FULL_MASK, suf_hi, 1) : 1.f;
+            if (lane == 31) R = ghi, R_hi = 1.f;
+            // entry f's value of a per-lane pair (lo: entries 0..31, hi: 32..63); f warp-uniform
+            auto entry_val = [&](float lo, float hv, int f) {
+                return f < 32 ? __shfl_sync(FULL_MASK, lo, f) : __shfl_sync(FULL_MASK, hv, f - 32);
+            };
 
             if (dots_here) {
                 // entry x (ring entry f = x < cpr, else window token s = x - cpr) against every window
@@ -584,7 +607,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                         v[TMAX + t] = b2.x + b2.y;
                     }
                     reduce_scatter_values<C::V, C::LPR>(v, pg);
-                    const float Rf = __shfl_sync(FULL_MASK, R, ring ? xc : 0);
+                    const int rsrc = ring ? xc : 0;  // differs between the warp's row groups
+                    float Rf = __shfl_sync(FULL_MASK, R, rsrc & 31);
+                    if (ring_hi) {
+                        const float rh = __shfl_sync(FULL_MASK, R_hi, rsrc & 31);
+                        if (rsrc >= 32) Rf = rh;
+                    }
                     if (x < J && pg % C::DUP == 0) {
 #pragma unroll
                         for (int i = 0; i < C::NVL; ++i) {
@@ -620,8 +648,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     for (int t = 1; t < TMAX; ++t)
                         if (lane == t) ikt = ikw[t];
                     const int64_t ent = unit_ring + (pos0 + lane) % L;
+                    // field 3: the call's window length on its first entry (what a rollback checks), else 0
                     *reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats) =
-                        make_float4(meta->alpha[lane], meta->beta[lane], ikt, 0.f);
+                        make_float4(meta->alpha[lane], meta->beta[lane], ikt, lane == 0 ? (float)T : 0.f);
                 }
             }
             if (appender && lane == 0) {
@@ -643,8 +672,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // Mamba2's skip weight (a flush, T = 0, has no outputs and no D)
                 const float dskip = RULE == RULE_MAMBA2 && T > 0 ? p.D[h] : 0.f;
                 const float g1 = fold ? 1.f : gring;  // decay of S0 to the window's first token
-                // fold: scale of entry f's rank-one term, R(f) / |k_f| (lane f)
+                // fold: scale of entry f's rank-one term, R(f) / |k_f| (lane f, entries 32 + f in fsc_hi)
                 const float fsc = lane < count ? R * rec[lane * rec_floats + 2] : 0.f;
+                const float fsc_hi = ring_hi && lane + 32 < count ? R_hi * rec[(lane + 32) * rec_floats + 2] : 0.f;
                 const float gfold = gring;
                 unsigned char* gck =
                     static_cast<unsigned char*>(p.ckpt) + ((int64_t)slot * p.Hv + h) * p.dv * MROW_BYTES;
@@ -655,6 +685,46 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                 // checkpoint and continue as the stored (rounded) values
                 auto fold_rows = [&](auto& s, const auto& j) {
                     constexpr int NR = sizeof(j) / sizeof(j[0]);
+                    if constexpr (MIXED) {
+                        // Two checkpoints: the recurrence runs on the master. Every buffered entry's raw
+                        // inputs go through the rule on the FP32 master rows, in order; a row's
+                        // prediction S^T k_f is a dot product within the row, so rows never wait for
+                        // one another. The raw key's inverse norm scales the dot product and the
+                        // correction instead of the key.
+                        for (int f = 0; f < count; ++f) {
+                            const float* rf = rec + f * rec_floats;
+                            const float alf = rf[0], bef = rf[1], ikf = rf[2];
+                            float kr[C::E];
+#pragma unroll
+                            for (int cc = 0; cc < C::NC; ++cc)
+                                load_run<C::VEC>(rk + f * DK * in_sz, pos_of(cc), in_dt, kr + cc * C::VEC);
+                            float u[NR];
+#pragma unroll
+                            for (int r = 0; r < NR; ++r) {
+                                float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int e = 0; e < C::E / 2; ++e)
+                                    d2 = __ffma2_rn(make_float2(s[r][2 * e], s[r][2 * e + 1]),
+                                                    make_float2(kr[2 * e], kr[2 * e + 1]), d2);
+                                u[r] = d2.x + d2.y;
+                            }
+#pragma unroll
+                            for (int r = 0; r < NR; ++r) u[r] = group_sum<C::LPR>(u[r]) * ikf;
+                            const float2 a2 = make_float2(alf, alf);
+#pragma unroll
+                            for (int r = 0; r < NR; ++r) {
+                                const float vf = load_elem(head + p.off_rv + f * p.dv * in_sz, j[r], in_dt);
+                                const float wk = bef * (vf - alf * u[r]) * ikf;
+                                const float2 w2 = make_float2(wk, wk);
+#pragma unroll
+                                for (int e = 0; e < C::E / 2; ++e) {
+                                    float2 t2 = __fmul2_rn(make_float2(s[r][2 * e], s[r][2 * e + 1]), a2);
+                                    t2 = __ffma2_rn(make_float2(kr[2 * e], kr[2 * e + 1]), w2, t2);
+                                    s[r][2 * e] = t2.x, s[r][2 * e + 1] = t2.y;
+                                }
+                            }
+                        }
+                    } else {
 #pragma unroll
                     for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -663,8 +733,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                     // takes the entries in order
                     for (int f = 0; f < count; f += 2) {
                         const bool two = f + 1 < count;
-                        const float sc0 = __shfl_sync(FULL_MASK, fsc, f);
-                        const float sc1 = two ? __shfl_sync(FULL_MASK, fsc, f + 1) : 0.f;
+                        const float sc0 = entry_val(fsc, fsc_hi, f);
+                        const float sc1 = two ? entry_val(fsc, fsc_hi, f + 1) : 0.f;
                         float k0[C::E], k1[C::E];
 #pragma unroll
                         for (int cc = 0; cc < C::NC; ++cc) {
@@ -684,6 +754,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) replay_kernel(const ReplayA
                                 s[r][2 * e] = t2.x, s[r][2 * e + 1] = t2.y;
                             }
                         }
+                    }
                     }
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {

@@ -60,21 +60,21 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 3
+#define GDN_ABI_VERSION 4
 
 /* Host-side return codes. */
 #define GDN_OK 0
 #define GDN_ERR_NULL (-1)    /* a required pointer is NULL */
 #define GDN_ERR_DTYPE (-2)   /* unsupported dtype or dtype mismatch */
 #define GDN_ERR_SHAPE (-3)   /* unsupported dk/dv, Hv % Hk != 0, negative sizes */
-#define GDN_ERR_WINDOW (-4)  /* T < 1, T > 8, T > L, L > 32 */
+#define GDN_ERR_WINDOW (-4)  /* T < 1, T > 8, T > L, L < 1 or L > 64 */
 #define GDN_ERR_ALIGN (-5)   /* a pointer is not 16-byte aligned */
 #define GDN_ERR_LAUNCH (-6)  /* CUDA reported an error at launch */
 
 /* Device-side error bits (set in *dev_err). */
 #define GDN_DEVERR_SLOT 1    /* slot index >= num_slots */
 #define GDN_DEVERR_RING 2    /* replay count pos - ckpt_pos outside [0, L], or a rollback below ckpt_pos */
-#define GDN_DEVERR_ACCEPT 4  /* accepted count outside [0, T-1] */
+#define GDN_DEVERR_ACCEPT 4  /* accepted count outside [0, T-1], or a rollback that does not undo a T-token window */
 #define GDN_DEVERR_TIMEOUT 8 /* an internal pipeline wait gave up (should never happen) */
 #define GDN_DEVERR_SEQLEN 16 /* prefill token offsets decreasing or beyond total_tokens */
 
@@ -149,18 +149,24 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
  * ring_k    [num_slots][Hv][L][dk] of ring_dtype: raw (unnormalised) keys.
  * ring_v    [num_slots][Hv][L][dv] of ring_dtype: raw values.
  * ring_rec  [num_slots][Hv][L][4 + dv] fp32: per entry {alpha, beta,
- *           1/|k|, 0, w[0..dv)}, where alpha and beta are the entry's gates,
- *           1/|k| = 1/sqrt(|k|^2 + 1e-6) its key's inverse norm and
- *           w = beta (v - alpha S_prev^T k) its correction vector (S_prev:
- *           the state just before the entry). 1/|k| and w are derived data
- *           the kernels keep so that an output needs one pass over S0, not
- *           one per buffered entry; w stays valid until the entry is folded.
- *           The ring is written only by these entry points.
+ *           1/|k|, n, w[0..dv)}, where alpha and beta are the entry's gates,
+ *           1/|k| = 1/sqrt(|k|^2 + 1e-6) its key's inverse norm,
+ *           n the length T of the call that appended it on that call's
+ *           first entry (0 on the others; gdn_rollback checks and clears
+ *           it), and w = beta (v - alpha S_prev^T k) its correction vector
+ *           (S_prev: the state just before the entry, as the outputs read
+ *           it). 1/|k| and w are derived data the kernels keep so that an
+ *           output needs one pass over S0, not one per buffered entry; w
+ *           stays valid until the entry is folded. The ring is written only
+ *           by these entry points; zero-filled is a valid initial ring.
  * pos       [num_slots][Hv] int32: absolute position of the next token.
  * ckpt_pos  [num_slots][Hv] int32: position the checkpoint corresponds to.
  *           count = pos - ckpt_pos entries are buffered, 0 <= count <= L;
  *           entry for absolute position t sits at ring index t mod L.
- * L         ring length, 1 <= L <= 32.
+ * L         ring length, 1 <= L <= 64. A shape whose ring, window and
+ *           checkpoint chunks cannot all be staged in one CTA's shared
+ *           memory is refused with GDN_ERR_SHAPE (with an fp32 checkpoint
+ *           and dk = 128: dv = 256 with L = 64 and T > 4).
  *
  * A fresh sequence: ckpt = its initial state, pos = ckpt_pos (any value >= 0).
  * A fold -- ckpt <- round(S after all buffered entries), ckpt_pos <- pos --
@@ -172,11 +178,15 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
  *            high-precision checkpoint for the recurrence and the
  *            low-precision copy for reading of the AREX ReplaySSM article
  *            (section "缓存输入而非状态", its precision paragraph). Every
- *            output and every prediction S^T k then reads ckpt_read; only a
- *            fold reads ckpt, applies the buffered entries' updates to it,
- *            stores it, and rewrites ckpt_read as the stored value rounded to
- *            read_dtype. A fresh sequence: ckpt_read = ckpt rounded. One
- *            launch per call: units that fold stream the fp32 checkpoint,
+ *            output, and every prediction S^T k between folds, then reads
+ *            ckpt_read; only a fold reads ckpt: it runs the buffered entries'
+ *            raw inputs through the rule on ckpt in FP32 -- every prediction
+ *            of the recurrence comes from the fp32 checkpoint itself --
+ *            stores it, and rewrites ckpt_read as the stored value rounded
+ *            to read_dtype. ckpt therefore evolves exactly as a
+ *            single-checkpoint replay with an fp32 checkpoint would. A fresh
+ *            sequence: ckpt_read = ckpt rounded. One launch per call: units
+ *            that fold stream the fp32 checkpoint and the buffered values,
  *            the others the read copy; the tokens of a call that folds run
  *            from the rewritten copy. Both arrays are 16-byte aligned and do
  *            not overlap.
@@ -230,10 +240,17 @@ int gdn_replay_flush(const gdn_dims* dims, const gdn_replay_cache* cache, const 
 
 /*
  * gdn_rollback -- after a T-token verify, keep 1 + accepted[b] tokens of
- * sequence b: pos[slot][h] -= T - 1 - accepted[b] for every head. A pure
- * pointer move (AREX ReplaySSM article: rollback becomes moving the buffer
- * pointer); no state or ring entry is touched.
+ * sequence b: pos[slot][h] -= T - 1 - accepted[b] for every head. A pointer
+ * move (AREX ReplaySSM article: rollback becomes moving the buffer pointer);
+ * no state, ring key, value, gate or w is touched.
  * accepted  [B] int32 device array, each in [0, T-1].
+ * T         must be the T of the gdn_verify_window call it undoes, with no
+ *           other replay call on those slots in between. Each (slot, h)
+ *           checks this against the window-length field of the window's
+ *           first ring record and clears that field, so a second rollback
+ *           of the same window is refused too: a mismatch sets
+ *           GDN_DEVERR_ACCEPT and leaves pos unchanged. A rollback below
+ *           ckpt_pos sets GDN_DEVERR_RING.
  */
 int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int32_t* slots,
                  const int32_t* accepted, int32_t T, int32_t* dev_err, void* stream);
@@ -303,7 +320,7 @@ int mamba2_decode_step(const mamba2_dims* dims, void* state_pool, int32_t state_
  * Folding, windows and rollback follow the gdn_replay_* rules exactly; the
  * read copy (ckpt_read) is not supported here (GDN_ERR_DTYPE).
  *   mamba2_replay_step    one token: out [B][H][P].
- *   mamba2_verify_window  T tokens, 1 <= T <= min(L, 8): x [B][T][H][P],
+ *   mamba2_verify_window  T tokens, 1 <= T <= min(L, 8), L <= 64: x [B][T][H][P],
  *                         dt [B][T][H], Bm, Cm [B][T][G][N], out [B][T][H][P].
  *   mamba2_replay_flush   fold full rings (or non-empty ones with force).
  *   mamba2_rollback       keep 1 + accepted[b] of the last window's T tokens.

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert gdn.gdn_abi_version() == 3
+    assert gdn.gdn_abi_version() == 4
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -115,7 +115,8 @@ def test_replay_rejections(lib):
     assert _verify(lib, d, _cache(L=16), 0) == -4  # GDN_ERR_WINDOW: T < 1
     assert _verify(lib, d, _cache(L=4), 5) == -4  # T > L
     assert _verify(lib, d, _cache(L=16), 9) == -4  # T > 8
-    assert _verify(lib, d, _cache(L=33), 4) == -4  # L > 32
+    assert _verify(lib, d, _cache(L=65), 4) == -4  # L > 64
+    assert lib.gdn_rollback(C.byref(d), C.byref(_cache(L=65)), FAKE, FAKE, 4, FAKE, None) == -4
     assert _verify(lib, d, _cache(L=0), 1) == -4
     assert _verify(lib, d, _cache(rdt=0), 4, idt=1) == -2  # input dtype differs from the ring's
     assert _verify(lib, d, _cache(cdt=5), 4) == -2

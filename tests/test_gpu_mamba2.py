@@ -221,13 +221,27 @@ def test_verify_and_rollback_small(T, L, sdt):
     H.check_state()
 
 
-def test_verify_at_the_largest_ring_window_and_head():
-    w = wl.Workload("m2x", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=6, state_dtype="f32", in_dtype="bf16", L=32, T=8,
+@pytest.mark.parametrize("sdt,L,P", [("f32", 32, 256), ("bf16", 64, 256), ("f32", 64, 128)])
+def test_verify_at_the_largest_ring_window_and_head(sdt, L, P):
+    # 20 rounds of T = 8 keep 1..8 tokens each: counts pass 32 and every ring folds
+    w = wl.Workload("m2x", B=3, Hk=1, Hv=2, dk=128, dv=P, steps=20, state_dtype=sdt, in_dtype="bf16", L=L, T=8,
                     seed=59)
     H = M2Harness(w)
     for r in range(w.steps):
         H.window(wl.mamba2_step_inputs(w, r), H.slots, 8, f"round {r}")
         H.rollback(wl.accepted(w, r), 8)
+    H.window(wl.mamba2_step_inputs(w.with_(T=1), 700), H.slots, 1, "step")
+    H.check_state()
+    assert all(hd.ckpt_pos > 0 for hd in H.heads.values())
+
+
+def test_single_steps_at_the_largest_ring():
+    # 64-entry rings folded by single steps: every fold takes all 64 entries
+    w = wl.Workload("m2l", B=3, Hk=1, Hv=2, dk=64, dv=32, steps=140, state_dtype="bf16", in_dtype="bf16", L=64,
+                    seed=60)
+    H = M2Harness(w)
+    for t in range(w.steps):
+        H.window(wl.mamba2_step_inputs(w, t), H.slots, 1, f"step {t}")
     H.check_state()
 
 

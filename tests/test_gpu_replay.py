@@ -108,7 +108,7 @@ class Harness:
 
 
 @pytest.mark.parametrize("sdt", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("L", [1, 4])
+@pytest.mark.parametrize("L", [1, 4, 64])
 def test_replay_steps_small_all_units(sdt, L):
     w = wl.Workload("rs", B=3, Hk=1, Hv=2, dk=32, dv=32, steps=3 * L + 5, state_dtype=sdt, in_dtype="f32", L=L,
                     seed=21)
@@ -153,16 +153,61 @@ def test_verify_and_rollback_small(T, L, sdt):
     H.check_state()
 
 
-@pytest.mark.parametrize("sdt", ["f32", "bf16"])
-def test_maximum_ring_window_and_head(sdt):
-    # the largest ring (L = 32), window (T = 8) and head (dk = 128, dv = 256) the entry points take
-    w = wl.Workload("mx", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=9, state_dtype=sdt, in_dtype="bf16", L=32, T=8,
+@pytest.mark.parametrize("sdt,L,dv,rdt", [("bf16", 64, 256, None), ("f32", 64, 128, None), ("f32", 32, 256, None),
+                                          ("f32", 55, 256, None), ("f32", 64, 128, "bf16")])
+def test_maximum_ring_window_and_head(sdt, L, dv, rdt):
+    # the largest ring (L = 64) and window (T = 8) with the largest head (dk = 128, dv = 256) where the
+    # unit's staging fits in shared memory; 20 rounds keep 1..8 tokens each, so counts pass 32 and fold
+    w = wl.Workload("mx", B=3, Hk=1, Hv=2, dk=128, dv=dv, steps=20, state_dtype=sdt, in_dtype="bf16", L=L, T=8,
                     seed=27)
-    H = Harness(w)
+    H = Harness(w, read_dtype=rdt)
+    most = 0
     for r in range(w.steps):
+        most = max(most, max(hd.count for hd in H.heads.values()))
         H.window(wl.step_inputs(w, r), H.slots, 8, f"round {r}")
         H.rollback(wl.accepted(w, r), 8)
     H.window(wl.step_inputs(w.with_(T=1), 700), H.slots, 1, "step")
+    H.check_state()
+    assert most > L - 16 and all(hd.ckpt_pos > 0 for hd in H.heads.values())
+
+
+def test_window_that_does_not_fit_is_refused():
+    # fp32 checkpoint, dk = 128, dv = 256: a T = 8 window's staging (8 chunks of the state, 64 ring
+    # entries of 1,040-byte records and the row-sum tiles) exceeds a CTA's shared memory
+    w = wl.Workload("mxr", B=2, Hk=1, Hv=2, dk=128, dv=256, steps=1, state_dtype="f32", in_dtype="bf16", L=64, T=8,
+                    seed=27)
+    H = Harness(w)
+    with pytest.raises(gdn.GdnError) as e:
+        H.window(wl.step_inputs(w, 0), H.slots, 8, "too big")
+    assert e.value.code == -3 and "shared memory" in str(e.value)
+
+
+def test_rollback_must_undo_the_last_window():
+    """gdn_rollback's T must be that of the window just verified. A mismatch, a second rollback of the
+    same window or a rollback after a plain step is refused -- GDN_DEVERR_ACCEPT, or GDN_DEVERR_RING
+    where the move would pass the checkpoint -- and moves no pointer."""
+    w = wl.Workload("rb", B=3, Hk=1, Hv=2, dk=32, dv=32, steps=3, state_dtype="f32", in_dtype="bf16", L=16, T=4,
+                    seed=29)
+    H = Harness(w)
+    c, s_d = H.g.cache, torch.from_numpy(H.slots).cuda()
+    acc0 = torch.from_numpy(wl.accepted(w, 0)).cuda()
+
+    def refused(T, bits=gdn.DEVERR_ACCEPT | gdn.DEVERR_RING):
+        before, err = c.pos.clone(), dev_err()
+        gdn.gdn_rollback(c, s_d, acc0, T, err)
+        torch.cuda.synchronize()
+        e = int(err.item())
+        assert e != 0 and e & ~bits == 0, e
+        assert torch.equal(c.pos, before)
+
+    H.window(wl.step_inputs(w, 0), H.slots, 4, "round 0")
+    refused(3, gdn.DEVERR_ACCEPT)  # the window had 4 tokens
+    H.rollback(wl.accepted(w, 0), 4)
+    refused(4)  # already rolled back
+    H.window(wl.step_inputs(w.with_(T=1), 900), H.slots, 1, "step")
+    refused(4)  # the last call was a single step
+    H.window(wl.step_inputs(w, 1), H.slots, 4, "round 1")
+    H.rollback(wl.accepted(w, 1), 4)
     H.check_state()
 
 
