@@ -38,6 +38,7 @@ L_RING, T_VERIFY = 16, 4
 # Mamba2 layer: groups, heads, state dim, head dim
 M2_G, M2_H, M2_N, M2_P = 8, 128, 128, 64
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, ~8 TB/s nominal
 KERNEL_SOURCES = ["gdn_decode.cuh", "gdn_device.cuh", "gdn_launch.cuh"]
 
 
@@ -103,13 +104,16 @@ def spec_bytes_per_seq(T: int, state_bytes: int, in_bytes: int = 2, out_bytes: i
 # ------------------------------------------------------------------ helpers
 
 
-def load_peaks() -> tuple[float, str]:
+def load_peaks() -> tuple[float, str, str]:
+    """The HBM peak fractions are taken against: the measured copy bandwidth of the GB300s
+    when MEASURED_PEAKS.json is present, else the fallback figure; with how it was measured."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", str(d.get("how", ""))[:160]
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, "fallback", "one earlier copy-bandwidth measurement on a GB300"
 
 
 def kernel_source_hash() -> str:
@@ -284,7 +288,7 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         launch = statistics.fmean(s.elapsed_time(e) for s, e in evs) if per_launch else elapsed / steps
         return max_over_ranks(elapsed), launch
 
-    peak, peak_kind = load_peaks()
+    peak, peak_kind, peak_how = load_peaks()
     result = {}
 
     # -------- headline: decode, fp32 state pool
@@ -310,7 +314,8 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
         "hbm_gbs": achieved,
         "bytes_per_token": bpt,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic(), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(), "peak_kind": peak_kind, "peak_how": peak_how,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "kernel": "gdn::decode_kernel<float, dk=128> (16 consumer warps in groups of 4, 6 chunk stages)",
                      "launch_us": launch_ms * 1e3,
                      "algorithmic_bytes_per_launch": bpt * B},
@@ -490,6 +495,10 @@ def gpu_arm(args, rank: int, world: int) -> dict | None:
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during the mode runs")
     result["modes"] = modes
+    result["drift"] = {"workload_decays": drift_modes(dev, gen, err, stream),
+                       "long_memory": drift_modes(dev, gen, err, stream, a_shift=-5.0)}
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during the drift runs")
     return result
 
 
@@ -611,13 +620,121 @@ def mamba2_modes(modes, timed, peak, args, world, dev, gen, err, stream) -> int:
     return launches
 
 
+def drift_modes(dev, gen, err, stream, steps: int = 200, a_shift: float = 0.0) -> dict:
+    """Low-precision drift on one token stream (untimed). B = 256 sequences, 32 heads, d = 128, bf16
+    activations, 200 steps from one common initial state (N(0, 0.1) in bf16, so every storage dtype
+    starts from the same values), through:
+      - decode with an fp32, bf16 and fp16 state pool (the state is rounded on every step);
+      - the ReplaySSM step (L = 16, every ring empty at the start) with a bf16 checkpoint, and with an
+        fp32 master checkpoint plus a bf16 read copy (the state is rounded only when the ring folds).
+    The reference is the fp32-state decode of the same stream, on every (sequence, head); the parity
+    tests check that run against the fp64 oracle within 1e-4 and the low-precision modes against the
+    oracle with the same rounding points. For each mode: the largest |output - reference| over all
+    steps, the RMS of that difference, the state after the last fold (or the final state, for decode)
+    against the reference state at the same position, and the requantisations of each (sequence,
+    head)'s stored state: one per step for decode, one per fold for replay, counted from the
+    checkpoint pointers the kernels move. The ReplaySSM article (section "缓存输入而非状态", its
+    precision paragraph) says replay requantises the low-precision checkpoint about L times less
+    often. a_shift is added to A_log: -5 gives decays of 0.97 to 0.99 per token, a long memory in
+    which roundings accumulate (the workload's own gates forget a rounding within a few tokens)."""
+    import torch
+
+    from hybrid_ssm_gated_gb300 import gdn
+    from hybrid_ssm_gated_gb300 import workload as wl
+
+    w = wl.WORKLOADS["decode_b256_bf16"]
+    A_log, dt_bias = (torch.from_numpy(t).to(dev) for t in wl.head_params(w))
+    A_log = A_log + a_shift
+    slots = torch.from_numpy(wl.slots(w)).to(dev)
+    sl = slots.long()
+    bf, f16, f32 = torch.bfloat16, torch.float16, torch.float32
+    S0 = (torch.randn(NUM_SLOTS, HV, DV, DK, generator=gen, device=dev) * 0.1).to(bf)
+    pools = {"fp32": S0.to(f32), "bf16": S0.clone(), "fp16": S0.to(f16)}
+    caches = {}
+    for name, cdt, rdt in (("bf16", bf, None), ("fp32_bf16copy", f32, bf)):
+        c = gdn.ReplayCache.allocate(NUM_SLOTS, HV, DK, DV, L_RING, cdt, bf, device=dev, read_dtype=rdt)
+        c.ckpt.copy_(S0.to(cdt))
+        if rdt is not None:
+            c.ckpt_read.copy_(S0)
+        caches[name] = c
+    modes = ["decode_bf16", "decode_fp16", "replay_bf16_ckpt", "replay_fp32_master_bf16_copy"]
+    outs = {m: torch.empty(B, HV, DV, device=dev) for m in ["decode_fp32"] + modes}
+    out_max = {m: torch.zeros((), device=dev) for m in modes}
+    out_sq = {m: torch.zeros((), dtype=torch.float64, device=dev) for m in modes}
+    folds = {m: torch.zeros((), dtype=torch.int64, device=dev) for m in modes[2:]}
+    snap = None  # the reference state after the last multiple of L tokens, where the last fold stands
+    for t in range(steps):
+        rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(bf)
+        q, k, v, a, b = rnd(B, HK, DK), rnd(B, HK, DK), rnd(B, HV, DV), rnd(B, HV), rnd(B, HV)
+        for m, p in (("decode_fp32", pools["fp32"]), ("decode_bf16", pools["bf16"]), ("decode_fp16", pools["fp16"])):
+            gdn.gdn_decode_step(p, slots, q, k, v, a, b, A_log, dt_bias, outs[m], err, stream)
+        for m, c in (("replay_bf16_ckpt", caches["bf16"]), ("replay_fp32_master_bf16_copy", caches["fp32_bf16copy"])):
+            before = c.ckpt_pos[sl].clone()
+            gdn.gdn_replay_step(c, slots, q, k, v, a, b, A_log, dt_bias, outs[m], err, stream)
+            folds[m] += (c.ckpt_pos[sl] != before).sum()
+        for m in modes:
+            d = outs[m] - outs["decode_fp32"]
+            out_max[m] = torch.maximum(out_max[m], d.abs().max())
+            out_sq[m] += (d.double() ** 2).sum()
+        if (t + 1) % L_RING == 0:
+            snap = pools["fp32"][sl].clone()
+    ref = pools["fp32"][sl]
+    units = B * HV
+    state = {
+        "decode_bf16": (pools["bf16"][sl].float() - ref).abs().max(),
+        "decode_fp16": (pools["fp16"][sl].float() - ref).abs().max(),
+        "replay_bf16_ckpt": (caches["bf16"].ckpt[sl].float() - snap).abs().max(),
+        "replay_fp32_master_bf16_copy": (caches["fp32_bf16copy"].ckpt_read[sl].float() - snap).abs().max(),
+    }
+    master = float((caches["fp32_bf16copy"].ckpt[sl] - snap).abs().max())
+    rep = {"steps": steps, "B": B, "L": L_RING, "A_log_shift": a_shift, "reference": "fp32-state decode of the same stream",
+           "fields": "out_max, out_rms, state_max vs the reference; requantisations per (sequence, head)"}
+    for m in modes:
+        rq = steps if m.startswith("decode") else float(folds[m]) / units
+        rep[m] = [float(f"{float(out_max[m]):.4g}"), float(f"{(float(out_sq[m]) / (units * DV * steps)) ** 0.5:.4g}"),
+                  float(f"{float(state[m]):.4g}"), rq]
+    rep["replay_fp32_master_bf16_copy_master_max"] = float(f"{master:.4g}")
+    rep["requant_ratio_decode_over_replay"] = float(f"{steps / rep['replay_bf16_ckpt'][3]:.4g}")
+    return rep
+
+
+def summary(res: dict) -> dict:
+    """Every configuration of the line in a few characters, the last key of the line."""
+    m = res["modes"]
+    peak = res["roofline"]["peak"]
+    g = lambda x: float(f"{x:.3g}")
+    f = lambda x: round(x, 3)
+    row = lambda tok, frac: [g(tok), f(frac), f(frac * peak / NOMINAL_HBM_GBS)]
+    s = {"fields": "tokens/s, frac of measured HBM peak, frac of nominal 8 TB/s (prefill: FP32 ALU frac)",
+         "decode_fp32": row(res["value"], res["roofline"]["frac"])}
+    for k, v in m.items():
+        tok = v.get("tokens_per_s", v.get("window_tokens_per_s"))
+        if k.startswith("prefill"):
+            s[k] = [g(tok), f(v["frac"])]
+        else:
+            s[k] = row(tok, v["frac"])
+        if "speedup_vs_decode" in v:
+            s[k].append(round(v["speedup_vs_decode"], 3))
+    d = res.get("drift")
+    if d:
+        s["drift_rms_out"] = {v: [d[v][k][1] for k in ("decode_bf16", "replay_bf16_ckpt",
+                                                       "replay_fp32_master_bf16_copy")] for v in d}
+        s["requant_decode_replay"] = [d["workload_decays"]["decode_bf16"][3],
+                                      d["workload_decays"]["replay_bf16_ckpt"][3]]
+    cb = res.get("cpu_baseline")
+    if cb:
+        s["oracle_tok_s"] = [g(cb["value"]), cb["cores"], g(cb.get("value_1_thread", 0.0))]
+    return s
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_decode_rate(seconds: float = 15.0, sample_seqs: int = 32) -> dict:
+def oracle_decode_rate(seconds: float = 15.0, sample_seqs: int = 32, seconds_1t: float = 5.0) -> dict:
     """Time the CPU oracle on a bounded sample of the headline workload:
     `sample_seqs` sequences x all 32 heads per step, steps repeated until
-    `seconds` of wall time, all host cores."""
+    `seconds` of wall time, all host cores; then the same on one thread for
+    about `seconds_1t`."""
     import numpy as np
 
     import oracle
@@ -639,10 +756,20 @@ def oracle_decode_rate(seconds: float = 15.0, sample_seqs: int = 32) -> dict:
     for x in xs:
         run(x)
     el = time.perf_counter() - ts
+    # one thread: a few steps of the same sample
+    run1 = lambda x: oracle.decode_step(pool, "f32", slots, x["q"], x["k"], x["v"], x["a"], x["b"], "bf16", A_log,
+                                        dt_bias, nthreads=1)
+    ts1 = time.perf_counter()
+    n1 = 0
+    while n1 < len(xs) and (n1 == 0 or time.perf_counter() - ts1 < seconds_1t):
+        run1(xs[n1])
+        n1 += 1
+    el1 = time.perf_counter() - ts1
     return {"value": sample_seqs * steps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{sample_seqs} sequences x {HV} heads x {steps} decode steps of the B=256 workload "
-                      f"(fp32 state, bf16 inputs), fp64 C oracle, OpenMP over (sequence, head)",
-            "seconds": el}
+            "sample": f"{sample_seqs} of the 256 sequences x {HV} heads x {steps} decode steps of the B=256 "
+                      f"workload (fp32 state, bf16 inputs), fp64 C oracle, OpenMP over (sequence, head)",
+            "seconds": el, "value_1_thread": sample_seqs * n1 / el1,
+            "sample_1_thread": f"the same sample, {n1} steps on one thread", "seconds_1_thread": el1}
 
 
 def reference_arm(args, rank: int, world: int) -> None:
@@ -681,8 +808,9 @@ def reference_arm(args, rank: int, world: int) -> None:
     el = time.perf_counter() - ts
     v = n * args.steps / el
     cb = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-          "sample": f"{n} sequences x {HV} heads per step of the B=256 workload (fp32 state, bf16 inputs), "
-                    f"{args.steps} timed steps after {args.warmup}, fp64 C oracle, OpenMP over (sequence, head)",
+          "sample": f"a sample of {n} of the 256 sequences x {HV} heads per step of the B=256 workload "
+                    f"(fp32 state, bf16 inputs), {args.steps} timed steps after {args.warmup}, fp64 C oracle, "
+                    f"OpenMP over (sequence, head); tokens/s counts the sampled sequences",
           "seconds": el}
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
@@ -832,6 +960,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = oracle_decode_rate()
+        res["summary"] = summary(res)  # last: a compact copy of every configuration's figures
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
