@@ -133,17 +133,12 @@ int replay_common(const char* fn, int rule, const gdn_dims* dims, const gdn_repl
     bool too_big = false;
     cudaError_t e;
     if (c->ckpt_read) {
-        // Two checkpoints, one launch: steps read the copy; folds stream the fp32 master, update it
-        // and rewrite the copy. A master chunk holds a whole number of the copy's chunks' items.
+        // Two checkpoints, one launch: steps read the copy; folds read the fp32 master, update it
+        // and rewrite the copy.
         p.ckpt_copy = c->ckpt_read;
-        chunking(dims->dk, dims->dv, gdn::dtype_size(c->read_dtype), p.rows, p.nchunk);
-        chunking(dims->dk, p.rows, 4, p.mrows, p.mnchunk);
-        p.mnchunk = dims->dv / p.mrows;
         e = c->read_dtype == GDN_BF16 ? gdn::dispatch_replay_f32_bf16(dims->dk, tmax, p, s, too_big)
                                       : gdn::dispatch_replay_f32_f16(dims->dk, tmax, p, s, too_big);
     } else if (rule == gdn::RULE_MAMBA2) {
-        chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
-        p.mrows = p.rows, p.mnchunk = p.nchunk;
         if (c->ckpt_dtype == GDN_F32)
             e = gdn::dispatch_mamba2_replay_f32(dims->dk, tmax, p, s, too_big);
         else if (c->ckpt_dtype == GDN_BF16)
@@ -151,8 +146,6 @@ int replay_common(const char* fn, int rule, const gdn_dims* dims, const gdn_repl
         else
             e = gdn::dispatch_mamba2_replay_f16(dims->dk, tmax, p, s, too_big);
     } else {
-        chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
-        p.mrows = p.rows, p.mnchunk = p.nchunk;
         if (c->ckpt_dtype == GDN_F32)
             e = gdn::dispatch_replay_f32(dims->dk, tmax, p, s, too_big);
         else if (c->ckpt_dtype == GDN_BF16)

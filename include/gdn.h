@@ -163,10 +163,7 @@ int gdn_spec_step(const gdn_dims* dims, void* state_pool, int32_t state_dtype, c
  * ckpt_pos  [num_slots][Hv] int32: position the checkpoint corresponds to.
  *           count = pos - ckpt_pos entries are buffered, 0 <= count <= L;
  *           entry for absolute position t sits at ring index t mod L.
- * L         ring length, 1 <= L <= 64. A shape whose ring, window and
- *           checkpoint chunks cannot all be staged in one CTA's shared
- *           memory is refused with GDN_ERR_SHAPE (with an fp32 checkpoint
- *           and dk = 128: dv = 256 with L = 64 and T > 4).
+ * L         ring length, 1 <= L <= 64.
  *
  * A fresh sequence: ckpt = its initial state, pos = ckpt_pos (any value >= 0).
  * A fold -- ckpt <- round(S after all buffered entries), ckpt_pos <- pos --
