@@ -3,6 +3,8 @@
 Each translation unit under csrc/ compiles in parallel; the objects are
 linked into hybrid_ssm_gated_gb300/lib/libgdn.so against the shared CUDA
 runtime. Rebuilds only when a source or header is newer than the library.
+build(debug=True) builds the bounds-checking variant (GDN_DEBUG_BOUNDS: every
+global copy and store checked against its array) into lib/debug/libgdn.so.
 """
 from __future__ import annotations
 
@@ -39,8 +41,14 @@ def _deps() -> list[str]:
         [os.path.join(INCLUDE, "gdn.h"), __file__]
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(LIBDIR, "obj", os.path.basename(src) + ".o")
+def _paths(debug: bool) -> tuple[str, str]:
+    """(library, object directory) of the normal or the bounds-checking build."""
+    d = os.path.join(LIBDIR, "debug") if debug else LIBDIR
+    return os.path.join(d, "libgdn.so"), os.path.join(d, "obj")
+
+
+def _compile(src: str, extra: list[str], objdir: str) -> str:
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     os.makedirs(os.path.dirname(obj), exist_ok=True)
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(d) for d in _deps()):
         return obj
@@ -54,23 +62,25 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link libgdn.so; returns its path."""
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Compile and link libgdn.so (debug: the bounds-checking build); returns its path."""
+    lib, objdir = _paths(debug)
+    os.makedirs(objdir, exist_ok=True)
     newest = max(os.path.getmtime(d) for d in _deps())
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
     if force:
-        shutil.rmtree(os.path.join(LIBDIR, "obj"), ignore_errors=True)
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), sources()))
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB + ".tmp"] + objs
+        shutil.rmtree(objdir, ignore_errors=True)
+        os.makedirs(objdir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + (["-DGDN_DEBUG_BOUNDS"] if debug else [])
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, extra, objdir), sources()))
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", lib + ".tmp"] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -119,6 +119,13 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
     __syncthreads();
 
     const int total = p.B * p.Hv;
+    // store extents, for the bounds-checking build
+    const uint64_t ext_state = (uint64_t)p.num_slots * p.Hv * p.dv * C::ROW_BYTES;
+    const uint64_t ext_out = (uint64_t)total * p.dv * dtype_size(p.out_dtype);
+    auto out_ok = [&](int64_t i) {
+        return in_bounds(static_cast<char*>(p.out) + i * dtype_size(p.out_dtype), dtype_size(p.out_dtype), p.out,
+                         ext_out, p.dev_err);
+    };
     const int in_sz = dtype_size(p.in_dtype);
     const int group = p.Hv / p.Hk;
 
@@ -132,6 +139,9 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
         const uint64_t pol = policy_evict_first();
         const uint32_t qbytes = DK * in_sz, vbytes = p.dv * in_sz;
         const uint32_t cbytes = p.rows * C::ROW_BYTES;
+        // source extents, for the bounds-checking build
+        const uint64_t ext_pool = (uint64_t)p.num_slots * p.Hv * p.dv * C::ROW_BYTES;
+        const uint64_t ext_qk = (uint64_t)p.B * p.Hk * qbytes, ext_v = (uint64_t)p.B * p.Hv * vbytes;
         uint32_t m = 0;   // chunk fills issued (one producer: all; several: up to the last one this warp issued)
         uint32_t nh = 0;  // head fills issued (likewise)
         uint32_t vb = 0;  // valid units in earlier batches
@@ -189,7 +199,10 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
                                           : lane == 1 ? static_cast<const char*>(p.k) + qrow * qbytes
                                                       : static_cast<const char*>(p.v) + (int64_t)unit * vbytes;
                         unsigned char* dst = head + (lane == 0 ? C::OFF_Q : lane == 1 ? C::OFF_K : C::OFF_V);
-                        if (lane < 3) bulk_load(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs]);
+                        if (lane < 3)
+                            bulk_load_checked(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs],
+                                              lane == 0 ? p.q : lane == 1 ? p.k : p.v, lane == 2 ? ext_v : ext_qk,
+                                              p.dev_err);
                     }
                     // this unit's first fill: after those of the valid units before it
                     const uint32_t m0 = (vb + __popc(valid & ((1u << i) - 1u))) * (uint32_t)p.nchunk;
@@ -203,7 +216,8 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
                                 const char* src = static_cast<const char*>(p.pool) +
                                                   ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)c * cbytes;
                                 mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                                bulk_load_hint_checked(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol, p.pool,
+                                                       ext_pool, p.dev_err);
                             }
                         }
                         ok = __all_sync(FULL_MASK, ok);
@@ -250,7 +264,10 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
                                           : lane == 1 ? static_cast<const char*>(p.k) + qrow * qbytes
                                                       : static_cast<const char*>(p.v) + (int64_t)unit * vbytes;
                         unsigned char* dst = head + (lane == 0 ? C::OFF_Q : lane == 1 ? C::OFF_K : C::OFF_V);
-                        if (lane < 3) bulk_load(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs]);
+                        if (lane < 3)
+                            bulk_load_checked(dst, src, lane == 2 ? vbytes : qbytes, &hfull[hs],
+                                              lane == 0 ? p.q : lane == 1 ? p.k : p.v, lane == 2 ? ext_v : ext_qk,
+                                              p.dev_err);
                     }
                     // then the chunks, each lane's as soon as its stage is free (a wait for every stage
                     // first delays the early chunks); at most NS lanes at a time, so no lane waits for a
@@ -265,7 +282,8 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
                                 const char* src = static_cast<const char*>(p.pool) +
                                                   ((int64_t)s_i * p.Hv + h) * p.dv * C::ROW_BYTES + (int64_t)c * cbytes;
                                 mbar_arrive_expect_tx(&cfull[cs], cbytes);
-                                bulk_load_hint(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol);
+                                bulk_load_hint_checked(chunks + cs * CHUNK_BYTES, src, cbytes, &cfull[cs], pol, p.pool,
+                                                       ext_pool, p.dev_err);
                             }
                         }
                         ok = __all_sync(FULL_MASK, ok);
@@ -305,7 +323,7 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
         const float dskip = reinterpret_cast<const float*>(head)[3];  // Mamba2's D[h]
         if (slot < 0) {
             for (int j = cw * 32 + lane; j < p.dv; j += NCW * 32)
-                store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, 0.f);
+                if (out_ok((int64_t)unit * p.dv + j)) store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, 0.f);
         } else {
             // A unit's passes go to one group of UW warps (groups alternate by unit), so each warp
             // normalises the window for only its group's units; every warp still waits for and
@@ -383,11 +401,12 @@ __global__ void __launch_bounds__((NCW + (sizeof(ST) == 2 ? 2 : 1)) * 32, 1) dec
                     char* dst = gstate + (int64_t)j * C::ROW_BYTES;
 #pragma unroll
                     for (int cc = 0; cc < C::NC; ++cc)
-                        *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = Store<ST>::pack(s + cc * C::VEC);
+                        if (in_bounds(dst + (cc * C::LPR + pg) * 16, 16, p.pool, ext_state, p.dev_err))
+                            *reinterpret_cast<uint4*>(dst + (cc * C::LPR + pg) * 16) = Store<ST>::pack(s + cc * C::VEC);
                     if (pg == 0) {
                         float o = fmaf(alpha, pq, qk * delta);
                         if constexpr (RULE == RULE_MAMBA2) o = fmaf(dskip, vj, o);
-                        store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, o);
+                        if (out_ok((int64_t)unit * p.dv + j)) store_elem(p.out, (int64_t)unit * p.dv + j, p.out_dtype, o);
                     }
                 }
                 __syncwarp();

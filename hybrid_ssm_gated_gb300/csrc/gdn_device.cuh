@@ -327,6 +327,53 @@ __device__ __forceinline__ void rule_gates(float A_log, float dt_bias, const voi
 
 __device__ __forceinline__ void set_error(int32_t* dev_err, int bits) { atomicOr(dev_err, bits); }
 
+// Complete `bytes` of a barrier's expected transaction with no copy. A bounds-checking build's
+// skipped bulk copy does this, so that the copy's waiters see the phase complete (and read stale
+// data, flagged by the error bit) instead of waiting out the timeout.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// Bounds-checking builds (compiled with GDN_DEBUG_BOUNDS): an access of `bytes` at `p` must lie in
+// [base, base + extent); otherwise GDN_DEVERR_BOUNDS is set and the caller skips the access, so a
+// wrong index shows as an error bit, never as a fault. In other builds the check is compiled out.
+__device__ __forceinline__ bool in_bounds(const void* p, uint64_t bytes, const void* base, uint64_t extent,
+                                          int32_t* dev_err) {
+#ifdef GDN_DEBUG_BOUNDS
+    const uint64_t a = reinterpret_cast<uint64_t>(p), b0 = reinterpret_cast<uint64_t>(base);
+    if (a < b0 || a + bytes > b0 + extent) {
+        set_error(dev_err, GDN_DEVERR_BOUNDS);
+        return false;
+    }
+#else
+    (void)p, (void)bytes, (void)base, (void)extent, (void)dev_err;
+#endif
+    return true;
+}
+
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+}  // namespace gdn
+
+namespace gdn {
+
+// Bulk copies with the bounds check of bounds-checking builds: the source range must lie in
+// [base, base + extent); a skipped copy completes its bytes on the barrier.
+__device__ __forceinline__ void bulk_load_checked(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                  const void* base, uint64_t extent, int32_t* dev_err) {
+    if (in_bounds(src, bytes, base, extent, dev_err))
+        bulk_load(dst, src, bytes, bar);
+    else
+        mbar_complete_tx(bar, bytes);
+}
+
+__device__ __forceinline__ void bulk_load_hint_checked(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                       uint64_t policy, const void* base, uint64_t extent,
+                                                       int32_t* dev_err) {
+    if (in_bounds(src, bytes, base, extent, dev_err))
+        bulk_load_hint(dst, src, bytes, bar, policy);
+    else
+        mbar_complete_tx(bar, bytes);
+}
 
 }  // namespace gdn

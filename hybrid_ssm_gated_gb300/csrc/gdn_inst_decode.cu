@@ -32,6 +32,7 @@ __global__ void rollback_kernel(int32_t* pos, const int32_t* ckpt_pos, float* ri
             continue;
         }
         float* mark = ring_rec + (idx * L + p0 % L) * (int64_t)rec_floats + 3;
+        if (!in_bounds(mark, 4, ring_rec, (uint64_t)num_slots * Hv * L * rec_floats * 4, dev_err)) continue;
         if (*mark != (float)T) {
             set_error(dev_err, GDN_DEVERR_ACCEPT);
             continue;

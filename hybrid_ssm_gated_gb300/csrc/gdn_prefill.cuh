@@ -104,13 +104,21 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
         return;
     }
     const int T = t1 - t0;
+    // array extents in bytes, for the bounds-checking build
+    const int osz = dtype_size(out_dt);
+    const uint64_t ext_out = (uint64_t)p.total * p.Hv * p.dv * osz;
+    const uint64_t ext_state = (uint64_t)p.num_slots * p.Hv * p.dv * C::ROW_BYTES;
+    const uint64_t ext_qk = (uint64_t)p.total * p.Hk * DK * dtype_size(in_dt);
+    const uint64_t ext_v = (uint64_t)p.total * p.Hv * p.dv * dtype_size(in_dt);
     const int row0 = rb * PF_ROWS;
     const int nrows = min(PF_ROWS, p.dv - row0);  // a multiple of 16
     if (slot < 0 || slot >= p.num_slots) {
         if (slot >= p.num_slots && threadIdx.x == 0 && rb == 0) set_error(p.dev_err, GDN_DEVERR_SLOT);
         for (int i = threadIdx.x; i < T * nrows; i += blockDim.x) {
             const int t = i / nrows, r = i - t * nrows;
-            store_elem(p.out, ((int64_t)(t0 + t) * p.Hv + h) * p.dv + row0 + r, out_dt, 0.f);
+            const int64_t oi = ((int64_t)(t0 + t) * p.Hv + h) * p.dv + row0 + r;
+            if (in_bounds(static_cast<char*>(p.out) + oi * osz, osz, p.out, ext_out, p.dev_err))
+                store_elem(p.out, oi, out_dt, 0.f);
         }
         return;
     }
@@ -138,16 +146,19 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             const int64_t tok = t0 + c * PF_TC + t;
             const char* src;
             unsigned char* d;
+            bool ok_;
             if (x < 2 * (qbytes / 16)) {
                 const int which = x / (qbytes / 16), piece = x - which * (qbytes / 16);
                 src = static_cast<const char*>(which ? p.k : p.q) + (tok * p.Hk + kh) * qbytes + piece * 16;
                 d = dst + (which * PF_TC + t) * qbytes + piece * 16;
+                ok_ = in_bounds(src, 16, which ? p.k : p.q, ext_qk, p.dev_err);
             } else {
                 const int piece = x - 2 * (qbytes / 16);
                 src = static_cast<const char*>(p.v) + ((tok * p.Hv + h) * p.dv + row0) * isz + piece * 16;
                 d = dst + 2 * PF_TC * qbytes + t * PF_ROWS * isz + piece * 16;
+                ok_ = in_bounds(src, 16, p.v, ext_v, p.dev_err);
             }
-            cp_async16(d, src);
+            if (ok_) cp_async16(d, src);
         }
         cp_async_commit();
     };
@@ -330,6 +341,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             const int t = i / q4, r = (i - t * q4) * 4;
             const float4 o = *reinterpret_cast<const float4*>(of + t * PF_ROWS + r);
             const int64_t oi = ((int64_t)(t0 + c * PF_TC + t) * p.Hv + h) * p.dv + row0 + r;
+            if (!in_bounds(static_cast<char*>(p.out) + oi * osz, 4 * osz, p.out, ext_out, p.dev_err)) continue;
             if (out_dt == GDN_F32) {
                 *reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi) = o;
             } else {
@@ -352,7 +364,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, GDN_PREFILL_MIN_BLOCKS) prefill
             for (int cc = 0; cc < C::NC; ++cc) {
 #pragma unroll
                 for (int e = 0; e < C::VEC; ++e) S[ps][cc * C::VEC + e] *= sig;
-                store_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
+                if (in_bounds(gstate + (int64_t)r * C::ROW_BYTES + pos_of(cc) * (int)sizeof(ST), C::VEC * sizeof(ST),
+                              p.pool, ext_state, p.dev_err))
+                    store_row_run<ST, C::VEC>(gstate + (int64_t)r * C::ROW_BYTES, pos_of(cc), S[ps] + cc * C::VEC);
             }
         }
     }

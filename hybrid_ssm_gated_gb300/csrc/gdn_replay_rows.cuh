@@ -121,6 +121,13 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
     const int group = p.Hv / p.Hk;
     const int rec_floats = 4 + p.dv;
     const int kbytes = DK * in_sz;
+    // array extents in bytes: every copy and store checks against them in bounds-checking builds
+    const uint64_t cells = (uint64_t)p.num_slots * p.Hv;
+    const uint64_t ext_ckpt = cells * p.dv * DK * SZ, ext_rk = cells * p.L * kbytes;
+    const uint64_t ext_rv = cells * p.L * p.dv * in_sz, ext_rec = cells * p.L * rec_floats * 4, ext_ptr = cells * 4;
+    const uint64_t ext_out = (uint64_t)p.B * p.T * p.Hv * p.dv * dtype_size(out_dt);
+    auto out_ok = [&](int64_t i) { return in_bounds(static_cast<char*>(p.out) + i * dtype_size(out_dt),
+                                                    dtype_size(out_dt), p.out, ext_out, p.dev_err); };
     const int nbat = (p.dv + 63) / 64;  // batches of 64 rows (the last may have 32)
     const int Q = nbat * NCH;           // sub-batches (batch, chunk) of a unit
     int dso[8];                         // the lane's stage pieces: row (lane / 4) + 8 m, piece lane % 4
@@ -195,7 +202,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         if (zero || skip) {
             for (int x = lane; zero && x < T * p.dv; x += 32) {
                 const int t = x / p.dv, j = x - t * p.dv;
-                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt, 0.f);
+                const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
+                if (out_ok(oi)) store_elem(p.out, oi, out_dt, 0.f);
             }
             unit = unit_next;
             continue;
@@ -219,7 +227,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
             const int npc = (p.dv - bq * 64 < 64 ? p.dv - bq * 64 : 64) / 4;  // 16-byte pieces of an entry
             for (int i = lane; i < count * npc; i += 32) {
                 const int f = i / npc, pc = i - f * npc;
-                cp_async_piece<16>(wcol + f * 64 + pc * 4, rec + ring_at(f) * rec_floats + 4 + bq * 64 + pc * 4);
+                const float* src = rec + ring_at(f) * rec_floats + 4 + bq * 64 + pc * 4;
+                if (in_bounds(src, 16, p.ring_rec, ext_rec, p.dev_err)) cp_async_piece<16>(wcol + f * 64 + pc * 4, src);
             }
         };
         auto issue = [&](int q) {
@@ -231,16 +240,21 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     const int r = (lane >> 2) + 8 * m;
-                    if (r < rows) cp_async_piece<16>(st + dso[m], src + (int64_t)r * SROW);
+                    if (r < rows && in_bounds(src + (int64_t)r * SROW, 16, p.ckpt, ext_ckpt, p.dev_err))
+                        cp_async_piece<16>(st + dso[m], src + (int64_t)r * SROW);
                 }
                 if (q == 0) {
-                    for (int f = lane; f < count; f += 32)
-                        cp_async_piece<16>(region + lay.hdr + f * 16, rec + ring_at(f) * rec_floats);
+                    for (int f = lane; f < count; f += 32) {
+                        const float* src = rec + ring_at(f) * rec_floats;
+                        if (in_bounds(src, 16, p.ring_rec, ext_rec, p.dev_err))
+                            cp_async_piece<16>(region + lay.hdr + f * 16, src);
+                    }
                     const int kp = kbytes / 16;
                     for (int i = lane; i < count * kp; i += 32) {
                         const int f = i / kp, k = i - f * kp;
-                        cp_async_piece<16>(keys + f * kbytes + k * 16, static_cast<const unsigned char*>(p.ring_k) +
-                                                                           (unit_ring + ring_at(f)) * kbytes + k * 16);
+                        const unsigned char* src =
+                            static_cast<const unsigned char*>(p.ring_k) + (unit_ring + ring_at(f)) * kbytes + k * 16;
+                        if (in_bounds(src, 16, p.ring_k, ext_rk, p.dev_err)) cp_async_piece<16>(keys + f * kbytes + k * 16, src);
                     }
                     issue_w(0);
                 }
@@ -478,7 +492,9 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     if (r == 1 && !row2) break;
                     unsigned char* dst = s0 + (int64_t)(j0 + 32 * r + lane) * SROW;
 #pragma unroll
-                    for (int v = 0; v < CE; v += 16 / SZ) st_state<ST, 16 / SZ>(dst, e0 + v, s[r] + v);
+                    for (int v = 0; v < CE; v += 16 / SZ)
+                        if (in_bounds(dst + (e0 + v) * SZ, 16, p.ckpt, ext_ckpt, p.dev_err))
+                            st_state<ST, 16 / SZ>(dst, e0 + v, s[r] + v);
                 }
                 if (T > 0) {
 #pragma unroll
@@ -573,7 +589,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     for (int x = 0; x < TMAX; ++x) {
                         if (x < T) {
                             const float wx = GDN ? bw[x] * (vx_pre[r][x] - aw[x] * y[x]) : bw[x] * vx_pre[r][x];
-                            rec[ri * rec_floats + 4 + j] = wx;
+                            if (in_bounds(rec + ri * rec_floats + 4 + j, 4, p.ring_rec, ext_rec, p.dev_err))
+                                rec[ri * rec_floats + 4 + j] = wx;
                             ri = ri + 1 == L ? 0 : ri + 1;
                             const float* cx = coef + (cpr + x) * C::CW;
 #pragma unroll
@@ -588,7 +605,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                         if (t < T) {
                             float o = z[t];
                             if constexpr (RULE == RULE_MAMBA2) o = fmaf(dskip, vx_pre[r][t], o);
-                            store_elem(p.out, out_b + t * out_t + j, out_dt, o);
+                            if (out_ok(out_b + t * out_t + j)) store_elem(p.out, out_b + t * out_t + j, out_dt, o);
                         }
                 }
             }
@@ -611,22 +628,26 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                 const int64_t qrow = ((int64_t)b * T + t) * p.Hk + kh;
                 const int64_t vrow = ((int64_t)b * T + t) * p.Hv + h;
                 for (int x = lane; x < kvec + vvec; x += 32) {
-                    if (x < kvec)
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * kbytes)[x] =
-                            reinterpret_cast<const uint4*>(static_cast<const char*>(p.k) + qrow * kbytes)[x];
-                    else
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz)[x - kvec] =
-                            reinterpret_cast<const uint4*>(static_cast<const char*>(p.v) + vrow * p.dv * in_sz)[x - kvec];
+                    if (x < kvec) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * kbytes) + x;
+                        if (in_bounds(dst, 16, p.ring_k, ext_rk, p.dev_err))
+                            *dst = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k) + qrow * kbytes)[x];
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz) + x - kvec;
+                        if (in_bounds(dst, 16, p.ring_v, ext_rv, p.dev_err))
+                            *dst = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v) + vrow * p.dv * in_sz)[x - kvec];
+                    }
                 }
             }
             if (lane < T) {
                 const int64_t ent = unit_ring + (pos0 + lane) % L;
                 // field 3: the call's window length on its first entry (what a rollback checks), else 0
-                *reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats) =
-                    make_float4(al_l, be_l, ik_l, lane == 0 ? (float)T : 0.f);
+                float4* dst = reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats);
+                if (in_bounds(dst, 16, p.ring_rec, ext_rec, p.dev_err))
+                    *dst = make_float4(al_l, be_l, ik_l, lane == 0 ? (float)T : 0.f);
             }
         }
-        if (lane == 0) {
+        if (lane == 0 && in_bounds(p.pos + uidx, 4, p.pos, ext_ptr, p.dev_err)) {
             p.pos[uidx] = pos0 + T;
             if (fold) p.ckpt_pos[uidx] = pos0;
         }

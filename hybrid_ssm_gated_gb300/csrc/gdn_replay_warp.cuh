@@ -286,6 +286,14 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
     const int group = p.Hv / p.Hk;
     const int rec_floats = 4 + p.dv;
     const int kbytes = DK * in_sz;           // a raw key row
+    // array extents in bytes: every copy and store checks against them in bounds-checking builds
+    const uint64_t cells = (uint64_t)p.num_slots * p.Hv;
+    const uint64_t ext_m = cells * p.dv * MROW, ext_s = cells * p.dv * SROW, ext_rk = cells * p.L * kbytes;
+    const uint64_t ext_rv = cells * p.L * p.dv * in_sz, ext_rec = cells * p.L * rec_floats * 4, ext_ptr = cells * 4;
+    const uint64_t ext_out = (uint64_t)p.B * p.T * p.Hv * p.dv * dtype_size(out_dt);
+    const void* sbase = MIXED ? p.ckpt_copy : p.ckpt;  // the checkpoint steps read
+    auto out_ok = [&](int64_t i) { return in_bounds(static_cast<char*>(p.out) + i * dtype_size(out_dt),
+                                                    dtype_size(out_dt), p.out, ext_out, p.dev_err); };
     const int Q = p.dv / 32 * SPB;           // sub-batches of a unit
     auto pos_of = [&](int c) { return (c * G + g) * VEC; };  // first element of the lane's c-th vector
 
@@ -359,7 +367,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
         if (zero || skip) {
             for (int x = lane; zero && x < T * p.dv; x += 32) {
                 const int t = x / p.dv, j = x - t * p.dv;
-                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt, 0.f);
+                const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
+                if (out_ok(oi)) store_elem(p.out, oi, out_dt, 0.f);
             }
             unit = unit_next;
             continue;
@@ -390,9 +399,11 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
 #pragma unroll
                     for (int u = 0; u < NSB; ++u)
 #pragma unroll
-                        for (int k = 0; k < NP; ++k)
-                            cp_async_piece<PS>(st + ((u * NP + k) * 32 + lane) * PS,
-                                               src + u * C::RPS * MROW + pos_of(k / PPV) * 4 + (k % PPV) * PS);
+                        for (int k = 0; k < NP; ++k) {
+                            const unsigned char* g_ = src + u * C::RPS * MROW + pos_of(k / PPV) * 4 + (k % PPV) * PS;
+                            if (in_bounds(g_, PS, p.ckpt, ext_m, p.dev_err))
+                                cp_async_piece<PS>(st + ((u * NP + k) * 32 + lane) * PS, g_);
+                        }
                 } else {
                     constexpr int SZ = (int)sizeof(ST);
                     constexpr int PS = VEC * SZ < 16 ? VEC * SZ : 16, PPV = VEC * SZ / PS, NP = C::NVEC * PPV;
@@ -400,19 +411,23 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
 #pragma unroll
                     for (int u = 0; u < NSB; ++u)
 #pragma unroll
-                        for (int k = 0; k < NP; ++k)
-                            cp_async_piece<PS>(st + ((u * NP + k) * 32 + lane) * PS,
-                                               src + u * C::RPS * SROW + pos_of(k / PPV) * SZ + (k % PPV) * PS);
+                        for (int k = 0; k < NP; ++k) {
+                            const unsigned char* g_ = src + u * C::RPS * SROW + pos_of(k / PPV) * SZ + (k % PPV) * PS;
+                            if (in_bounds(g_, PS, sbase, ext_s, p.dev_err))
+                                cp_async_piece<PS>(st + ((u * NP + k) * 32 + lane) * PS, g_);
+                        }
                 }
                 if (q == 0) {
-                    for (int f = lane; f < count; f += 32)
-                        cp_async_piece<16>(region + lay.hdr + f * 16, rec + ring_at(f) * rec_floats);
+                    for (int f = lane; f < count; f += 32) {
+                        const float* g_ = rec + ring_at(f) * rec_floats;
+                        if (in_bounds(g_, 16, p.ring_rec, ext_rec, p.dev_err)) cp_async_piece<16>(region + lay.hdr + f * 16, g_);
+                    }
                     const int kp = kbytes / 16;
                     for (int i = lane; i < count * kp; i += 32) {
                         const int f = i / kp, k = i - f * kp;
-                        cp_async_piece<16>(keys + f * kbytes + k * 16,
-                                           static_cast<const unsigned char*>(p.ring_k) +
-                                               (unit_ring + ring_at(f)) * kbytes + k * 16);
+                        const unsigned char* g_ =
+                            static_cast<const unsigned char*>(p.ring_k) + (unit_ring + ring_at(f)) * kbytes + k * 16;
+                        if (in_bounds(g_, 16, p.ring_k, ext_rk, p.dev_err)) cp_async_piece<16>(keys + f * kbytes + k * 16, g_);
                     }
                 }
                 if (q % SPB == 0) {
@@ -421,13 +436,17 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                     if (fm) {
                         // 4 bytes holding column col of every entry's raw v (and its pair's, 16-bit)
                         const int pair = in_sz == 4 ? col : (col & ~1);
-                        for (int f = 0; f < count; ++f)
-                            cp_async_piece<4>(vcol + (buf * L + f) * 32 + lane,
-                                              static_cast<const unsigned char*>(p.ring_v) +
-                                                  ((unit_ring + ring_at(f)) * p.dv + pair) * in_sz);
+                        for (int f = 0; f < count; ++f) {
+                            const unsigned char* g_ = static_cast<const unsigned char*>(p.ring_v) +
+                                                      ((unit_ring + ring_at(f)) * p.dv + pair) * in_sz;
+                            if (in_bounds(g_, 4, p.ring_v, ext_rv, p.dev_err))
+                                cp_async_piece<4>(vcol + (buf * L + f) * 32 + lane, g_);
+                        }
                     } else {
-                        for (int f = 0; f < count; ++f)
-                            cp_async_piece<4>(wcol + (buf * L + f) * 32 + lane, rec + ring_at(f) * rec_floats + 4 + col);
+                        for (int f = 0; f < count; ++f) {
+                            const float* g_ = rec + ring_at(f) * rec_floats + 4 + col;
+                            if (in_bounds(g_, 4, p.ring_rec, ext_rec, p.dev_err)) cp_async_piece<4>(wcol + (buf * L + f) * 32 + lane, g_);
+                        }
                     }
                 }
             }
@@ -640,8 +659,13 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                 for (int u = 0; u < NSB; ++u)
 #pragma unroll
                     for (int c = 0; c < C::NVEC; ++c) {
-                        st_state<MT, VEC>(mck + jr[u] * MROW, pos_of(c), st[u] + c * VEC);
-                        if constexpr (MIXED) st_state<ST, VEC>(cck + jr[u] * SROW, pos_of(c), st[u] + c * VEC);
+                        if (in_bounds(mck + jr[u] * MROW + pos_of(c) * (int)sizeof(MT), VEC * sizeof(MT), p.ckpt, ext_m,
+                                      p.dev_err))
+                            st_state<MT, VEC>(mck + jr[u] * MROW, pos_of(c), st[u] + c * VEC);
+                        if constexpr (MIXED)
+                            if (in_bounds(cck + jr[u] * SROW + pos_of(c) * (int)sizeof(ST), VEC * sizeof(ST), sbase, ext_s,
+                                          p.dev_err))
+                                st_state<ST, VEC>(cck + jr[u] * SROW, pos_of(c), st[u] + c * VEC);
                     }
             }
             if (T == 0) continue;
@@ -778,7 +802,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                 for (int x = 0; x < TMAX; ++x) {
                     if (x < T) {
                         const float wx = GDN ? bw[x] * (vx_pre[x] - aw[x] * y[x]) : bw[x] * vx_pre[x];
-                        rec[ri * rec_floats + 4 + j] = wx;
+                        if (in_bounds(rec + ri * rec_floats + 4 + j, 4, p.ring_rec, ext_rec, p.dev_err))
+                            rec[ri * rec_floats + 4 + j] = wx;
                         ri = ri + 1 == L ? 0 : ri + 1;
                         const float* cx = coef + (cpr + x) * C::CW;
 #pragma unroll
@@ -794,7 +819,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                     if (t < T) {
                         float o = z[t];
                         if constexpr (RULE == RULE_MAMBA2) o = fmaf(dskip, vx_pre[t], o);
-                        store_elem(p.out, out_b + t * out_t + j, out_dt, o);
+                        if (out_ok(out_b + t * out_t + j)) store_elem(p.out, out_b + t * out_t + j, out_dt, o);
                     }
             }
             __syncwarp();  // the tile is free for the next batch
@@ -811,22 +836,26 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                 const int64_t qrow = ((int64_t)b * T + t) * p.Hk + kh;
                 const int64_t vrow = ((int64_t)b * T + t) * p.Hv + h;
                 for (int x = lane; x < kvec + vvec; x += 32) {
-                    if (x < kvec)
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * kbytes)[x] =
-                            reinterpret_cast<const uint4*>(static_cast<const char*>(p.k) + qrow * kbytes)[x];
-                    else
-                        reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz)[x - kvec] =
-                            reinterpret_cast<const uint4*>(static_cast<const char*>(p.v) + vrow * p.dv * in_sz)[x - kvec];
+                    if (x < kvec) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.ring_k) + ent * kbytes) + x;
+                        if (in_bounds(dst, 16, p.ring_k, ext_rk, p.dev_err))
+                            *dst = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k) + qrow * kbytes)[x];
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.ring_v) + ent * p.dv * in_sz) + x - kvec;
+                        if (in_bounds(dst, 16, p.ring_v, ext_rv, p.dev_err))
+                            *dst = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v) + vrow * p.dv * in_sz)[x - kvec];
+                    }
                 }
             }
             if (lane < T) {
                 const int64_t ent = unit_ring + (pos0 + lane) % L;
                 // field 3: the call's window length on its first entry (what a rollback checks), else 0
-                *reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats) =
-                    make_float4(al_l, be_l, ik_l, lane == 0 ? (float)T : 0.f);
+                float4* dst = reinterpret_cast<float4*>(p.ring_rec + ent * rec_floats);
+                if (in_bounds(dst, 16, p.ring_rec, ext_rec, p.dev_err))
+                    *dst = make_float4(al_l, be_l, ik_l, lane == 0 ? (float)T : 0.f);
             }
         }
-        if (lane == 0) {
+        if (lane == 0 && in_bounds(p.pos + uidx, 4, p.pos, ext_ptr, p.dev_err)) {
             p.pos[uidx] = pos0 + T;
             if (fold) p.ckpt_pos[uidx] = pos0;
         }

@@ -106,6 +106,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
     const int in_sz = dtype_size(in_dt);
     const int group = p.Hv / p.Hk;
     const int T = p.T;
+    // array extents in bytes, for the bounds-checking build
+    const uint64_t ext_pool = (uint64_t)p.num_slots * p.Hv * p.dv * C::ROW_BYTES;
+    const uint64_t ext_qk = (uint64_t)p.B * T * p.Hk * DK * in_sz, ext_v = (uint64_t)p.B * T * p.Hv * p.dv * in_sz;
+    const uint64_t ext_out = (uint64_t)p.B * T * p.Hv * p.dv * dtype_size(out_dt);
+    auto out_ok = [&](int64_t i) {
+        return in_bounds(static_cast<char*>(p.out) + i * dtype_size(out_dt), dtype_size(out_dt), p.out, ext_out,
+                         p.dev_err);
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
@@ -192,6 +200,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                     unsigned char* dstp = nullptr;
                     uint32_t bytes = 0;
                     uint64_t* bar = &hfull[hs];
+                    const void* sbase = p.pool;  // the source's array and its extent (bounds-checking builds)
+                    uint64_t sext = ext_pool;
                     if (round == 0 && lane < hj) {
                         const int t = lane / 3, kind = lane - 3 * t;
                         const int64_t qrow = ((int64_t)b * T + t) * p.Hk + kh;
@@ -202,6 +212,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                         dstp = head + (kind == 0 ? p.off_q + t * qbytes : kind == 1 ? p.off_k + t * qbytes
                                                                                     : p.off_v + t * vbytes);
                         bytes = kind == 2 ? vbytes : qbytes;
+                        sbase = kind == 0 ? p.q : kind == 1 ? p.k : p.v;
+                        sext = kind == 2 ? ext_v : ext_qk;
                     }
                     const int c = c0 + lane - cl0;
                     if (lane >= cl0 && lane - cl0 < per && c < p.nchunk) {
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                         }
                     }
                     ok = __all_sync(FULL_MASK, ok);
-                    if (ok && bytes) bulk_load_hint(dstp, srcp, bytes, bar, pol);
+                    if (ok && bytes) bulk_load_hint_checked(dstp, srcp, bytes, bar, pol, sbase, sext, p.dev_err);
                     c0 += per;
                 }
                 m += p.nchunk;
@@ -256,7 +268,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
         if (src < 0) {
             for (int x = cw * 32 + lane; x < T * p.dv; x += NCW * 32) {
                 const int t = x / p.dv, j = x - t * p.dv;
-                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt, 0.f);
+                const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
+                if (out_ok(oi)) store_elem(p.out, oi, out_dt, 0.f);
             }
         } else {
             // the window's keys and queries, normalised, at this lane's key positions; q_t.k_t
@@ -327,16 +340,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) spec_kernel(const SpecArgs 
                                     __ffma2_rn(kw2[t][e], d2, __fmul2_rn(make_float2(s[2 * e], s[2 * e + 1]), al2));
                                 s[2 * e] = r2.x, s[2 * e + 1] = r2.y;
                             }
-                            if (pg == 0)
-                                store_elem(p.out, (((int64_t)b * T + t) * p.Hv + h) * p.dv + j, out_dt,
-                                           fmaf(alpha, pq, qk[t] * delta));
+                            const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
+                            if (pg == 0 && out_ok(oi)) store_elem(p.out, oi, out_dt, fmaf(alpha, pq, qk[t] * delta));
                             const int d = meta->dst[t];
                             if (d >= 0) {  // this token's state copy, rounded once
                                 char* dst = static_cast<char*>(p.pool) + (((int64_t)d * p.Hv + h) * p.dv + j) * C::ROW_BYTES;
 #pragma unroll
                                 for (int cc = 0; cc < C::NC; ++cc)
-                                    *reinterpret_cast<uint4*>(dst + pos_of(cc) * (int)sizeof(ST)) =
-                                        Store<ST>::pack(s + cc * C::VEC);
+                                    if (in_bounds(dst + pos_of(cc) * (int)sizeof(ST), 16, p.pool, ext_pool, p.dev_err))
+                                        *reinterpret_cast<uint4*>(dst + pos_of(cc) * (int)sizeof(ST)) =
+                                            Store<ST>::pack(s + cc * C::VEC);
                             }
                         }
                     }

@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gdn.h")
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
-DEVERR_SLOT, DEVERR_RING, DEVERR_ACCEPT, DEVERR_TIMEOUT, DEVERR_SEQLEN = 1, 2, 4, 8, 16
+DEVERR_SLOT, DEVERR_RING, DEVERR_ACCEPT, DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_BOUNDS = 1, 2, 4, 8, 16, 32
 
 
 class GdnError(RuntimeError):
@@ -70,12 +70,15 @@ _SIGS = {
 
 
 def lib() -> C.CDLL:
-    """The loaded libgdn.so (built by hybrid_ssm_gated_gb300.build.build())."""
+    """The loaded libgdn.so (built by hybrid_ssm_gated_gb300.build.build()). The environment variable
+    GDN_LIBRARY names another build of it to load instead, such as the bounds-checking one
+    (build.build(debug=True))."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with hybrid_ssm_gated_gb300.build.build()")
-        lib_ = C.CDLL(LIB_PATH)
+        path = LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with hybrid_ssm_gated_gb300.build.build()")
+        lib_ = C.CDLL(path)
         for name, args in _SIGS.items():
             fn = getattr(lib_, name)
             fn.argtypes = args

@@ -77,6 +77,8 @@ extern "C" {
 #define GDN_DEVERR_ACCEPT 4  /* accepted count outside [0, T-1], or a rollback that does not undo a T-token window */
 #define GDN_DEVERR_TIMEOUT 8 /* an internal pipeline wait gave up (should never happen) */
 #define GDN_DEVERR_SEQLEN 16 /* prefill token offsets decreasing or beyond total_tokens */
+#define GDN_DEVERR_BOUNDS 32 /* bounds-checking builds only (GDN_DEBUG_BOUNDS): a copy or store fell
+                                outside its array and was skipped */
 
 /* Element types of states, activations and outputs; mirrors the fp32 /
  * bf16 / fp16 choice of a mamba SSM cache dtype. */

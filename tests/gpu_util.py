@@ -54,14 +54,40 @@ def maxabs(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64)))) if np.size(a) else 0.0
 
 
+GUARD = 256  # bytes of poisoned canary before and after a guarded array
+POISON = 0xA5
+
+
+def guarded(shape, dtype, keep: list) -> torch.Tensor:
+    """A zeroed CUDA tensor with GUARD poisoned bytes before and after it in the same allocation (its
+    storage is appended to `keep`, for canaries_intact)."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    raw = torch.full((n + 2 * GUARD,), POISON, dtype=torch.uint8, device="cuda")
+    t = raw[GUARD:GUARD + n].view(dtype).view(shape)
+    t.zero_()
+    keep.append(raw)
+    return t
+
+
+def canaries_intact(keep: list) -> bool:
+    """Every guarded tensor's poisoned bytes are unchanged: no kernel wrote just outside an array."""
+    torch.cuda.synchronize()
+    return all(bool((r[:GUARD] == POISON).all()) and bool((r[-GUARD:] == POISON).all()) for r in keep)
+
+
 class GpuReplay:
-    """A ReplaySSM cache on the GPU built from a workload's initial pool."""
+    """A ReplaySSM cache on the GPU built from a workload's initial pool; every array of it sits
+    between poisoned canary bytes (check with canaries_intact(self.guards))."""
 
     def __init__(self, w: wl.Workload, pool_host: np.ndarray, read_dtype=None):
         num_slots = pool_host.shape[0]
-        self.cache = gdn.ReplayCache.allocate(num_slots, w.Hv, w.dk, w.dv, w.L, TORCH_DT[w.state_dtype],
-                                              TORCH_DT[w.in_dtype],
-                                              read_dtype=None if read_dtype is None else TORCH_DT[read_dtype])
+        self.guards = []
+        g = lambda shape, dt: guarded(shape, dt, self.guards)
+        sdt, idt = TORCH_DT[w.state_dtype], TORCH_DT[w.in_dtype]
+        S = (num_slots, w.Hv)
+        self.cache = gdn.ReplayCache(g(S + (w.dv, w.dk), sdt), g(S + (w.L, w.dk), idt), g(S + (w.L, w.dv), idt),
+                                     g(S + (w.L, 4 + w.dv), torch.float32), g(S, torch.int32), g(S, torch.int32), w.L,
+                                     None if read_dtype is None else g(S + (w.dv, w.dk), TORCH_DT[read_dtype]))
         self.cache.ckpt.copy_(dev(pool_host, w.state_dtype))
         if read_dtype is not None:  # a fresh sequence's read copy is its checkpoint rounded
             self.cache.ckpt_read.copy_(dev(oracle.round_to(oracle.load(pool_host, w.state_dtype), read_dtype),

@@ -15,7 +15,8 @@ import torch
 import oracle
 from hybrid_ssm_gated_gb300 import build, gdn
 from hybrid_ssm_gated_gb300 import workload as wl
-from tests.gpu_util import TOL, TORCH_DT, GpuReplay, dev, dev_err, maxabs, sample_units, step_to_device, to_f64
+from tests.gpu_util import (TOL, TORCH_DT, GpuReplay, canaries_intact, dev, dev_err, guarded, maxabs, sample_units,
+                            step_to_device, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -109,7 +110,9 @@ class M2Harness:
     def window(self, x: dict, slots: np.ndarray, T: int, label: str):
         w = self.w
         xd = step_to_device(x, w.in_dtype)
-        out = torch.full((w.B, T, w.Hv, w.dv), 3.0, device="cuda")
+        og = []  # the output's canaries, checked after the call
+        out = guarded((w.B, T, w.Hv, w.dv), torch.float32, og)
+        out.fill_(3.0)
         s_d = torch.from_numpy(slots).cuda()
         if T == 1:
             gdn.mamba2_replay_step(self.g.cache, s_d, xd["x"], xd["dt"], xd["Bm"], xd["Cm"], self.A_d, self.dt_d,
@@ -118,6 +121,7 @@ class M2Harness:
             gdn.mamba2_verify_window(self.g.cache, s_d, xd["x"], xd["dt"], xd["Bm"], xd["Cm"], self.A_d, self.dt_d,
                                      self.D_d, out, self.err)
         got = to_f64(out)
+        assert canaries_intact(og), f"{label}: a kernel wrote outside the output"
         per = w.Hv // w.Hk
         for (b, h) in self.units:
             if slots[b] < 0:
@@ -167,6 +171,7 @@ class M2Harness:
                 assert rec[s, h, i, 1] == pytest.approx(hd.ed[e], rel=1e-5, abs=1e-30)
                 assert rec[s, h, i, 2] == 1.0
         assert int(self.err.item()) == 0
+        assert canaries_intact(self.g.guards), "a kernel wrote outside a cache array"
 
 
 @pytest.mark.parametrize("sdt,idt", [("f32", "f32"), ("bf16", "bf16"), ("f16", "bf16")])

@@ -17,8 +17,8 @@ import torch
 import oracle
 from hybrid_ssm_gated_gb300 import build, gdn
 from hybrid_ssm_gated_gb300 import workload as wl
-from tests.gpu_util import (TOL, TORCH_DT, GpuReplay, dev, dev_err, maxabs, oracle_window, replay_oracle_heads,
-                            sample_units, step_to_device, to_f64)
+from tests.gpu_util import (TOL, TORCH_DT, GpuReplay, canaries_intact, dev, dev_err, guarded, maxabs, oracle_window,
+                            replay_oracle_heads, sample_units, step_to_device, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,9 @@ class Harness:
     def window(self, x: dict, slots: np.ndarray, T: int, label: str):
         w = self.w
         xd = step_to_device(x, w.in_dtype)
-        out = torch.full((w.B, T, w.Hv, w.dv), 3.0, device="cuda")
+        og = []  # the output's canaries, checked after the call
+        out = guarded((w.B, T, w.Hv, w.dv), torch.float32, og)
+        out.fill_(3.0)
         s_d = torch.from_numpy(slots).cuda()
         if T == 1:
             gdn.gdn_replay_step(self.g.cache, s_d, xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], self.A_d, self.dt_d,
@@ -58,6 +60,7 @@ class Harness:
             gdn.gdn_verify_window(self.g.cache, s_d, xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], self.A_d, self.dt_d,
                                   out, self.err)
         got = to_f64(out)
+        assert canaries_intact(og), f"{label}: a kernel wrote outside the output"
         for (b, h) in self.units:
             if slots[b] < 0:
                 assert np.all(got[b, :, h] == 0.0)
@@ -105,6 +108,7 @@ class Harness:
                 assert rec[s, h, i, 0] == pytest.approx(hd.ea[e], rel=1e-5, abs=1e-30)
                 assert rec[s, h, i, 1] == pytest.approx(hd.eb[e], rel=1e-5, abs=1e-30)
         assert int(self.err.item()) == 0
+        assert canaries_intact(self.g.guards), "a kernel wrote outside a cache array or an output"
 
 
 @pytest.mark.parametrize("sdt", ["f32", "bf16", "f16"])
