@@ -32,6 +32,9 @@
 
 namespace gdn {
 
+constexpr int ROWS_ROUND = 256;                          // units a CTA lists per round
+constexpr int ROWS_SMEM_HEAD = 16 + 2 * ROWS_ROUND * 16;  // the round's counters and lists
+
 template <typename ST, int DK, int TMAX, int RULE>
 struct RowsCfg {
     static constexpr int SZ = (int)sizeof(ST);
@@ -47,7 +50,8 @@ struct RowsCfg {
 };
 
 // One warp's shared memory: the copy stages; the window's normalised keys and queries [TMAX][DK]
-// each; the buffered raw keys [L][DK] and record headers {alpha, beta, 1/|k|, n} [L]; the current
+// each; the buffered keys [L][DK], normalised fp32 (staged raw at the end of their region and
+// converted in place), and record headers {alpha, beta, 1/|k|, n} [L]; the current
 // batch's 64 columns of every buffered entry's w [L][64]; the coefficient table [L + TMAX][CW].
 struct RowsLayout {
     int stage, kwin, qwin, keys, hdr, wcol, coef, bytes;
@@ -61,7 +65,7 @@ __host__ __device__ constexpr RowsLayout replay_rows_layout(int L, int in_sz) {
     w.kwin = C::NS * C::STAGE;
     w.qwin = w.kwin + TMAX * DK * 4;
     w.keys = w.qwin + TMAX * DK * 4;
-    w.hdr = w.keys + align_up(L * DK * in_sz, 16);
+    w.hdr = w.keys + L * DK * 4;
     w.wcol = w.hdr + L * 16;
     w.coef = w.wcol + L * 64 * 4;
     w.bytes = align_up(w.coef + (L + TMAX) * C::CW * 4, 16);
@@ -101,20 +105,23 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
     constexpr int EPL = DK / 32;  // key elements per lane in the warp-wide dot products
     const int in_dt = io_in<IO>(p.in_dtype), out_dt = io_out<IO>(p.out_dtype);
     const int in_sz = dtype_size(in_dt);
+    // dynamic shared memory: the round's counters and unit lists, then one region per warp
     extern __shared__ __align__(128) unsigned char smem[];
-    int& next_unit = *reinterpret_cast<int*>(smem);
+    int* ctr = reinterpret_cast<int*>(smem);              // next list index; folds listed; others listed
+    int4* lfold = reinterpret_cast<int4*>(smem + 16);     // {unit, slot, pos, ckpt_pos} of the fold units
+    int4* lrest = lfold + ROWS_ROUND;                     // ... and of the others
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RowsLayout lay = replay_rows_layout<ST, DK, TMAX, RULE>(p.L, in_sz);
-    unsigned char* region = smem + REPLAY_SMEM_HEAD + warp * lay.bytes;
+    unsigned char* region = smem + ROWS_SMEM_HEAD + warp * lay.bytes;
     unsigned char* stages = region + lay.stage;
     float* kwin = reinterpret_cast<float*>(region + lay.kwin);  // [TMAX][DK] normalised window keys
     float* qwin = reinterpret_cast<float*>(region + lay.qwin);  // [TMAX][DK] normalised, scaled queries
-    unsigned char* keys = region + lay.keys;                    // [L][DK] buffered raw keys
+    unsigned char* keys = region + lay.keys;                    // [L][DK] buffered keys
+    float* keysf = reinterpret_cast<float*>(keys);               // ... normalised, once converted
+    const int rawoff = p.L * DK * 4 - p.L * DK * in_sz;          // where the raw keys are staged
     const float4* hdr = reinterpret_cast<const float4*>(region + lay.hdr);
     float* wcol = reinterpret_cast<float*>(region + lay.wcol);  // [L][64] w of the batch's columns
     float* coef = reinterpret_cast<float*>(region + lay.coef);  // [entry][CW]: S^T k at [t], S^T q at [TMAX + t]
-    if (threadIdx.x == 0) next_unit = 0;
-    __syncthreads();
 
     const int total = p.B * p.Hv;
     const int T = p.T, L = p.L;
@@ -134,23 +141,39 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
 #pragma unroll
     for (int m = 0; m < 8; ++m) dso[m] = rows_piece((lane >> 2) + 8 * m, lane & 3);
 
-    auto grab = [&]() {
-        int n = 0;
-        if (lane == 0) n = atomicAdd(&next_unit, 1);
-        return blockIdx.x + __shfl_sync(FULL_MASK, n, 0) * gridDim.x;
-    };
-    int unit = grab();
-    int slot_n = unit < total ? p.slots[unit / p.Hv] : -1;
-    int pos_n = 0, ck_n = 0;
-    bool ptrs_n = false;
-    while (unit < total) {
+    // The CTA's units blockIdx.x + n * gridDim.x go in rounds of ROWS_ROUND. A round starts with every
+    // thread loading one unit's slot and pointers and listing it, fold units first; then the warps
+    // take the list's units one at a time, so the heavier fold units never trail a round.
+    const int per_cta = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    for (int r0 = 0; r0 < per_cta; r0 += ROWS_ROUND) {
+    const int nr = per_cta - r0 < ROWS_ROUND ? per_cta - r0 : ROWS_ROUND;
+    if (threadIdx.x == 0) ctr[0] = ctr[1] = ctr[2] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+        const int u = blockIdx.x + (r0 + i) * gridDim.x;
+        const int sl = p.slots[u / p.Hv];
+        int ps = 0, ck = 0;
+        bool heavy = false;  // folds (whether its pointers are valid is checked when it is run)
+        if (sl >= 0 && sl < p.num_slots) {
+            const int64_t idx = (int64_t)sl * p.Hv + (u - u / p.Hv * p.Hv);
+            ps = p.pos[idx], ck = p.ckpt_pos[idx];
+            heavy = T > 0 ? ps - ck + T > L : (p.force ? ps - ck > 0 : ps - ck + 1 > L);
+        }
+        if (heavy)
+            lfold[atomicAdd(&ctr[1], 1)] = make_int4(u, sl, ps, ck);
+        else
+            lrest[atomicAdd(&ctr[2], 1)] = make_int4(u, sl, ps, ck);
+    }
+    __syncthreads();
+    const int nf = ctr[1];
+    for (;;) {
+        int li = 0;
+        if (lane == 0) li = atomicAdd(&ctr[0], 1);
+        li = __shfl_sync(FULL_MASK, li, 0);
+        if (li >= nr) break;
+        const int4 ent = li < nf ? lfold[li] : lrest[li - nf];
+        const int unit = ent.x, slot = ent.y, pos0 = ent.z, ck0 = ent.w;
         const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
-        const int slot = slot_n;
-        int pos0 = pos_n, ck0 = ck_n;
-        const bool have_ptrs = ptrs_n;
-        const int unit_next = grab();
-        ptrs_n = false;
-        slot_n = unit_next < total ? p.slots[unit_next / p.Hv] : -1;
 
         // ------------------------------------------------ the window's raw inputs (independent of the slot)
         float kr[TMAX][EPL], qr[TMAX][EPL];  // lane's EPL consecutive elements of each token's key, query
@@ -183,11 +206,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         } else if (slot < 0) {
             zero = true;
         } else {
-            if (!have_ptrs) {
-                const int64_t idx = (int64_t)slot * p.Hv + h;
-                pos0 = p.pos[idx];
-                ck0 = p.ckpt_pos[idx];
-            }
             count = pos0 - ck0;
             if (ck0 < 0 || count < 0 || count > L) {
                 if (lane == 0) set_error(p.dev_err, GDN_DEVERR_RING);
@@ -205,7 +223,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                 const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
                 if (out_ok(oi)) store_elem(p.out, oi, out_dt, 0.f);
             }
-            unit = unit_next;
             continue;
         }
         const int cpr = fold ? 0 : count;  // ring entries in front of the window
@@ -254,7 +271,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                         const int f = i / kp, k = i - f * kp;
                         const unsigned char* src =
                             static_cast<const unsigned char*>(p.ring_k) + (unit_ring + ring_at(f)) * kbytes + k * 16;
-                        if (in_bounds(src, 16, p.ring_k, ext_rk, p.dev_err)) cp_async_piece<16>(keys + f * kbytes + k * 16, src);
+                        if (in_bounds(src, 16, p.ring_k, ext_rk, p.dev_err))
+                            cp_async_piece<16>(keys + rawoff + f * kbytes + k * 16, src);
                     }
                     issue_w(0);
                 }
@@ -337,14 +355,21 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         R = __shfl_down_sync(FULL_MASK, suf, 1);
         R_hi = ring_hi ? __shfl_down_sync(FULL_MASK, suf_hi, 1) : 1.f;
         if (lane == 31) R = ghi, R_hi = 1.f;
-        fsc = lane < count ? R * hdr[lane].z : 0.f;
-        fsc_hi = ring_hi && lane + 32 < count ? R_hi * hdr[lane + 32].z : 0.f;
-        if (slot_n >= 0 && slot_n < p.num_slots) {  // the next unit's pointers
-            const int64_t ni = (int64_t)slot_n * p.Hv + (unit_next - unit_next / p.Hv * p.Hv);
-            pos_n = p.pos[ni];
-            ck_n = p.ckpt_pos[ni];
-            ptrs_n = true;
+        fsc = lane < count ? R : 0.f;
+        fsc_hi = ring_hi && lane + 32 < count ? R_hi : 0.f;
+        // the buffered keys to normalised fp32, in entry order: the fp32 row of entry f overlaps only the
+        // raw rows of entries up to f, so each entry's raw elements are read (by all lanes) before its
+        // fp32 row is written
+        for (int f = 0; f < count; ++f) {
+            const float ik = hdr[f].z;
+            float kv[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) kv[e] = load_elem(keys + rawoff + f * kbytes, lane * EPL + e, in_dt) * ik;
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) keysf[f * DK + lane * EPL + e] = kv[e];
         }
+        __syncwarp();
         if (T > 0) {
             // ------------------------------ coefficient table
             // entry x (ring entry f = x < cpr, else window token s = x - cpr) against every window
@@ -365,10 +390,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     const int x = x0 + i < J ? x0 + i : J - 1;
                     float kx[EPL];
                     if (x < cpr) {
-                        const float ikf = hdr[x].z;
 #pragma unroll
-                        for (int e = 0; e < EPL; ++e)
-                            kx[e] = load_elem(keys + x * kbytes, lane * EPL + e, in_dt) * ikf;
+                        for (int e = 0; e < EPL; ++e) kx[e] = keysf[x * DK + lane * EPL + e];
                     } else {
 #pragma unroll
                         for (int e = 0; e < EPL; ++e) kx[e] = kwin[(x - cpr) * DK + lane * EPL + e];
@@ -457,8 +480,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                 __syncwarp();
             }
             if (fold) {
-                // S0 <- G S0 + sum_f A(f) k_f w_f^T on the lane's rows of this chunk, stored rounded; the
-                // dot products below then read the stored values
+                // S0 <- G S0 + sum_f A(f) k_f w_f^T on the lane's rows of this chunk (k_f normalised),
+                // stored rounded; the dot products below then read the stored values
                 float s[2][CE];
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
@@ -476,9 +499,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     const float2 w1 = make_float2(w1s, w1s);
 #pragma unroll
                     for (int g4 = 0; g4 < CE / 4; ++g4) {
-                        float kf[4];
-                        load_run<4>(keys + f * kbytes, e0 + 4 * g4, in_dt, kf);
-                        const float2 k01 = make_float2(kf[0], kf[1]), k23 = make_float2(kf[2], kf[3]);
+                        const float4 kf = *reinterpret_cast<const float4*>(keysf + f * DK + e0 + 4 * g4);
+                        const float2 k01 = make_float2(kf.x, kf.y), k23 = make_float2(kf.z, kf.w);
                         float2 a = make_float2(s[0][4 * g4], s[0][4 * g4 + 1]), c = make_float2(s[0][4 * g4 + 2], s[0][4 * g4 + 3]);
                         a = __ffma2_rn(k01, w0, a), c = __ffma2_rn(k23, w0, c);
                         s[0][4 * g4] = a.x, s[0][4 * g4 + 1] = a.y, s[0][4 * g4 + 2] = c.x, s[0][4 * g4 + 3] = c.y;
@@ -561,49 +583,63 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
             if (T > 0) {
                 const float G1 = fold ? 1.f : gring;  // decay of S0 to the window's first token
                 const float dskip = RULE == RULE_MAMBA2 ? p.D[h] : 0.f;
+                // both rows at once, so that each coefficient is loaded once (a batch of 32 rows leaves
+                // the second row's values unused)
+                float y[2][TMAX], z[2][TMAX];
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) {
+                        y[r][t] = GDN ? (acc[r][t].x + acc[r][t].y) * (G1 * Pk[t]) : 0.f;
+                        const float2 aq = acc[r][(GDN ? TMAX : 0) + t];
+                        z[r][t] = (aq.x + aq.y) * (G1 * Pq[t]);
+                    }
+                // the buffered entries' terms (their w staged with the batch)
+                for (int f = 0; f < cpr; ++f) {
+                    const float w0 = wcol[f * 64 + lane], w1 = wcol[f * 64 + 32 + lane];
+                    const float* cf = coef + f * C::CW;
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) {
+                        if constexpr (GDN) {
+                            const float ck = cf[t];
+                            y[0][t] = fmaf(ck, w0, y[0][t]), y[1][t] = fmaf(ck, w1, y[1][t]);
+                        }
+                        const float cq = cf[TMAX + t];
+                        z[0][t] = fmaf(cq, w0, z[0][t]), z[1][t] = fmaf(cq, w1, z[1][t]);
+                    }
+                }
+                // the window: w_x, then its terms in the later sums of the rows
+                int ri = pos0 % L;
+#pragma unroll
+                for (int x = 0; x < TMAX; ++x) {
+                    if (x < T) {
+                        float wx[2];
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            wx[r] = GDN ? bw[x] * (vx_pre[r][x] - aw[x] * y[r][x]) : bw[x] * vx_pre[r][x];
+                            float* dst = rec + ri * rec_floats + 4 + j0 + 32 * r + lane;
+                            if ((r == 0 || row2) && in_bounds(dst, 4, p.ring_rec, ext_rec, p.dev_err)) *dst = wx[r];
+                        }
+                        ri = ri + 1 == L ? 0 : ri + 1;
+                        const float* cx = coef + (cpr + x) * C::CW;
+#pragma unroll
+                        for (int t = 0; t < TMAX; ++t) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                if constexpr (GDN) y[r][t] = fmaf(cx[t], wx[r], y[r][t]);
+                                z[r][t] = fmaf(cx[TMAX + t], wx[r], z[r][t]);
+                            }
+                        }
+                    }
+                }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (r == 1 && !row2) break;
                     const int j = j0 + 32 * r + lane;
-                    float y[TMAX], z[TMAX];
-#pragma unroll
-                    for (int t = 0; t < TMAX; ++t) {
-                        y[t] = GDN ? (acc[r][t].x + acc[r][t].y) * (G1 * Pk[t]) : 0.f;
-                        const float2 aq = acc[r][(GDN ? TMAX : 0) + t];
-                        z[t] = (aq.x + aq.y) * (G1 * Pq[t]);
-                    }
-                    // the buffered entries' terms (their w staged with the batch)
-                    const float* wc = wcol + 32 * r + lane;
-                    for (int f = 0; f < cpr; ++f) {
-                        const float wf = wc[f * 64];
-                        const float* cf = coef + f * C::CW;
-#pragma unroll
-                        for (int t = 0; t < TMAX; ++t) {
-                            if constexpr (GDN) y[t] = fmaf(cf[t], wf, y[t]);
-                            z[t] = fmaf(cf[TMAX + t], wf, z[t]);
-                        }
-                    }
-                    // the window: w_x, then its terms in the later sums of the row
-                    int ri = pos0 % L;
-#pragma unroll
-                    for (int x = 0; x < TMAX; ++x) {
-                        if (x < T) {
-                            const float wx = GDN ? bw[x] * (vx_pre[r][x] - aw[x] * y[x]) : bw[x] * vx_pre[r][x];
-                            if (in_bounds(rec + ri * rec_floats + 4 + j, 4, p.ring_rec, ext_rec, p.dev_err))
-                                rec[ri * rec_floats + 4 + j] = wx;
-                            ri = ri + 1 == L ? 0 : ri + 1;
-                            const float* cx = coef + (cpr + x) * C::CW;
-#pragma unroll
-                            for (int t = 0; t < TMAX; ++t) {
-                                if constexpr (GDN) y[t] = fmaf(cx[t], wx, y[t]);
-                                z[t] = fmaf(cx[TMAX + t], wx, z[t]);
-                            }
-                        }
-                    }
 #pragma unroll
                     for (int t = 0; t < TMAX; ++t)
                         if (t < T) {
-                            float o = z[t];
+                            float o = z[r][t];
                             if constexpr (RULE == RULE_MAMBA2) o = fmaf(dskip, vx_pre[r][t], o);
                             if (out_ok(out_b + t * out_t + j)) store_elem(p.out, out_b + t * out_t + j, out_dt, o);
                         }
@@ -651,7 +687,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
             p.pos[uidx] = pos0 + T;
             if (fold) p.ckpt_pos[uidx] = pos0;
         }
-        unit = unit_next;
+    }
+    __syncthreads();  // the next round rewrites the lists
     }
 }
 
