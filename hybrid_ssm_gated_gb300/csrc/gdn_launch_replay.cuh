@@ -55,12 +55,11 @@ cudaError_t launch_replay(ReplayArgs& a, cudaStream_t stream, bool& too_big) {
     // as many of the NW warps as the per-warp shared memory allows (fewer only for long rings)
     const int wb = MIXED ? replay_warp_layout<ST, MT, DK, TMAX, RULE>(a.L, dtype_size(a.in_dtype)).bytes
                          : replay_rows_layout<ST, DK, TMAX, RULE>(a.L, dtype_size(a.in_dtype)).bytes;
-    int nw = (di.smem_optin - (MIXED ? REPLAY_SMEM_HEAD : ROWS_SMEM_HEAD)) / wb;
+    int nw = (di.smem_optin - REPLAY_SMEM_HEAD) / wb;
     if (nw > NW) nw = NW;
     too_big = nw < 1;
     if (too_big) return cudaSuccess;
-    const int head = MIXED ? REPLAY_SMEM_HEAD : ROWS_SMEM_HEAD;
-    const int smem = head + nw * wb;
+    const int smem = REPLAY_SMEM_HEAD + nw * wb;
     int bps = 0;
     if ((e = prepare_kernel(kern, nw * 32, smem, bps)) != cudaSuccess) return e;
     const int units = a.B * a.Hv;

@@ -32,9 +32,6 @@
 
 namespace gdn {
 
-constexpr int ROWS_ROUND = 256;                          // units a CTA lists per round
-constexpr int ROWS_SMEM_HEAD = 16 + 2 * ROWS_ROUND * 16;  // the round's counters and lists
-
 template <typename ST, int DK, int TMAX, int RULE>
 struct RowsCfg {
     static constexpr int SZ = (int)sizeof(ST);
@@ -109,10 +106,10 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
     extern __shared__ __align__(128) unsigned char smem[];
     int* ctr = reinterpret_cast<int*>(smem);              // next list index; folds listed; others listed
     int4* lfold = reinterpret_cast<int4*>(smem + 16);     // {unit, slot, pos, ckpt_pos} of the fold units
-    int4* lrest = lfold + ROWS_ROUND;                     // ... and of the others
+    int4* lrest = lfold + REPLAY_ROUND;                   // ... and of the others
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RowsLayout lay = replay_rows_layout<ST, DK, TMAX, RULE>(p.L, in_sz);
-    unsigned char* region = smem + ROWS_SMEM_HEAD + warp * lay.bytes;
+    unsigned char* region = smem + REPLAY_SMEM_HEAD + warp * lay.bytes;
     unsigned char* stages = region + lay.stage;
     float* kwin = reinterpret_cast<float*>(region + lay.kwin);  // [TMAX][DK] normalised window keys
     float* qwin = reinterpret_cast<float*>(region + lay.qwin);  // [TMAX][DK] normalised, scaled queries
@@ -141,30 +138,11 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
 #pragma unroll
     for (int m = 0; m < 8; ++m) dso[m] = rows_piece((lane >> 2) + 8 * m, lane & 3);
 
-    // The CTA's units blockIdx.x + n * gridDim.x go in rounds of ROWS_ROUND. A round starts with every
-    // thread loading one unit's slot and pointers and listing it, fold units first; then the warps
-    // take the list's units one at a time, so the heavier fold units never trail a round.
+    // the CTA's units, in rounds of listed units, fold units first (REPLAY_ROUND, gdn_replay_warp.cuh)
     const int per_cta = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-    for (int r0 = 0; r0 < per_cta; r0 += ROWS_ROUND) {
-    const int nr = per_cta - r0 < ROWS_ROUND ? per_cta - r0 : ROWS_ROUND;
-    if (threadIdx.x == 0) ctr[0] = ctr[1] = ctr[2] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-        const int u = blockIdx.x + (r0 + i) * gridDim.x;
-        const int sl = p.slots[u / p.Hv];
-        int ps = 0, ck = 0;
-        bool heavy = false;  // folds (whether its pointers are valid is checked when it is run)
-        if (sl >= 0 && sl < p.num_slots) {
-            const int64_t idx = (int64_t)sl * p.Hv + (u - u / p.Hv * p.Hv);
-            ps = p.pos[idx], ck = p.ckpt_pos[idx];
-            heavy = T > 0 ? ps - ck + T > L : (p.force ? ps - ck > 0 : ps - ck + 1 > L);
-        }
-        if (heavy)
-            lfold[atomicAdd(&ctr[1], 1)] = make_int4(u, sl, ps, ck);
-        else
-            lrest[atomicAdd(&ctr[2], 1)] = make_int4(u, sl, ps, ck);
-    }
-    __syncthreads();
+    for (int r0 = 0; r0 < per_cta; r0 += REPLAY_ROUND) {
+    const int nr = per_cta - r0 < REPLAY_ROUND ? per_cta - r0 : REPLAY_ROUND;
+    replay_list_round(p, T, L, r0, nr, ctr, lfold, lrest);
     const int nf = ctr[1];
     for (;;) {
         int li = 0;

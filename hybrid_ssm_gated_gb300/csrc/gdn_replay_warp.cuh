@@ -227,7 +227,13 @@ struct WarpCfg {
     static_assert(DK % E == 0 && G >= 1 && G <= 32 && NSET % NSB == 0 && NS >= 2, "unsupported dk");
 };
 
-constexpr int REPLAY_SMEM_HEAD = 16;  // bytes of the CTA's unit counter, before the warps' regions
+// Unit scheduling of both replay kernels: a CTA takes its units blockIdx.x + n * gridDim.x in rounds
+// of REPLAY_ROUND. A round starts with every thread loading one unit's slot and pointers and listing
+// the unit, fold units first; then the warps take the list's units one at a time from a counter, so
+// the heavier fold units never trail a round and no warp waits on a unit's pointer loads. The head of
+// the dynamic shared memory holds the counters and the two lists.
+constexpr int REPLAY_ROUND = 256;
+constexpr int REPLAY_SMEM_HEAD = 16 + 2 * REPLAY_ROUND * 16;
 
 // One warp's shared memory, 16-byte aligned pieces: the copy stages; the staged ring columns of the
 // current batch (w, and for two-checkpoint folds the raw values v; double-buffered by batch); the
@@ -252,6 +258,31 @@ __host__ __device__ constexpr WarpLayout replay_warp_layout(int L, int in_sz) {
     return w;
 }
 
+// One round's unit lists (REPLAY_ROUND, above): units blockIdx.x + (r0 + i) * gridDim.x, i < nr, as
+// {unit, slot, pos, ckpt_pos}, fold units in lfold (ctr[1] of them), the others in lrest (ctr[2]);
+// ctr[0], the warps' next list index, starts at 0. Called by every thread of the CTA.
+__device__ __forceinline__ void replay_list_round(const ReplayArgs& p, int T, int L, int r0, int nr, int* ctr,
+                                                  int4* lfold, int4* lrest) {
+    if (threadIdx.x == 0) ctr[0] = ctr[1] = ctr[2] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+        const int u = blockIdx.x + (r0 + i) * gridDim.x;
+        const int sl = p.slots[u / p.Hv];
+        int ps = 0, ck = 0;
+        bool heavy = false;  // folds (whether its pointers are valid is checked when it is run)
+        if (sl >= 0 && sl < p.num_slots) {
+            const int64_t idx = (int64_t)sl * p.Hv + (u - u / p.Hv * p.Hv);
+            ps = p.pos[idx], ck = p.ckpt_pos[idx];
+            heavy = T > 0 ? ps - ck + T > L : (p.force ? ps - ck > 0 : ps - ck + 1 > L);
+        }
+        if (heavy)
+            lfold[atomicAdd(&ctr[1], 1)] = make_int4(u, sl, ps, ck);
+        else
+            lrest[atomicAdd(&ctr[2], 1)] = make_int4(u, sl, ps, ck);
+    }
+    __syncthreads();
+}
+
 // ST: the checkpoint that steps and windows read (the read copy in the two-checkpoint mode);
 // MT: the checkpoint that folds read and write (ST itself with one checkpoint).
 template <typename ST, int DK, int TMAX, int NW, typename MT = ST, int RULE = RULE_GDN, int IO = IO_ANY>
@@ -265,7 +296,9 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
     const int in_sz = dtype_size(in_dt);
     // dynamic shared memory: the unit counter, then one region per warp
     extern __shared__ __align__(128) unsigned char smem[];
-    int& next_unit = *reinterpret_cast<int*>(smem);
+    int* ctr = reinterpret_cast<int*>(smem);              // next list index; folds listed; others listed
+    int4* lfold = reinterpret_cast<int4*>(smem + 16);     // {unit, slot, pos, ckpt_pos} of the fold units
+    int4* lrest = lfold + REPLAY_ROUND;                   // ... and of the others
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane % G;   // lane's place in its row group
     const int rg = lane / G;  // row group within the warp
@@ -278,8 +311,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
     const float4* hdr = reinterpret_cast<const float4*>(region + lay.hdr);  // [L] {alpha, beta, 1/|k|, n}
     float* tile = reinterpret_cast<float*>(region + lay.tile);
     float* coef = reinterpret_cast<float*>(region + lay.coef);  // [entry][CW]: S^T k at [t], S^T q at [TMAX + t]
-    if (threadIdx.x == 0) next_unit = 0;
-    __syncthreads();
 
     const int total = p.B * p.Hv;
     const int T = p.T, L = p.L;
@@ -297,24 +328,19 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
     const int Q = p.dv / 32 * SPB;           // sub-batches of a unit
     auto pos_of = [&](int c) { return (c * G + g) * VEC; };  // first element of the lane's c-th vector
 
-    auto grab = [&]() {
-        int n = 0;
-        if (lane == 0) n = atomicAdd(&next_unit, 1);
-        return blockIdx.x + __shfl_sync(FULL_MASK, n, 0) * gridDim.x;
-    };
-    // the next unit's slot (and, once known, its pointers) load while the current one runs
-    int unit = grab();
-    int slot_n = unit < total ? p.slots[unit / p.Hv] : -1;
-    int pos_n = 0, ck_n = 0;
-    bool ptrs_n = false;
-    while (unit < total) {
+    const int per_cta = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    for (int r0 = 0; r0 < per_cta; r0 += REPLAY_ROUND) {
+    const int nr = per_cta - r0 < REPLAY_ROUND ? per_cta - r0 : REPLAY_ROUND;
+    replay_list_round(p, T, L, r0, nr, ctr, lfold, lrest);
+    const int nf = ctr[1];
+    for (;;) {
+        int li = 0;
+        if (lane == 0) li = atomicAdd(&ctr[0], 1);
+        li = __shfl_sync(FULL_MASK, li, 0);
+        if (li >= nr) break;
+        const int4 ent = li < nf ? lfold[li] : lrest[li - nf];
+        const int unit = ent.x, slot = ent.y, pos0 = ent.z, ck0 = ent.w;
         const int b = unit / p.Hv, h = unit - b * p.Hv, kh = h / group;
-        const int slot = slot_n;
-        int pos0 = pos_n, ck0 = ck_n;
-        const bool have_ptrs = ptrs_n;
-        const int unit_next = grab();
-        ptrs_n = false;
-        slot_n = unit_next < total ? p.slots[unit_next / p.Hv] : -1;
 
         // ------------------------------------------------ the window's raw inputs (independent of the slot)
         float kw[TMAX][E], qw[TMAX][E];
@@ -348,11 +374,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
         } else if (slot < 0) {
             zero = true;
         } else {
-            if (!have_ptrs) {
-                const int64_t idx = (int64_t)slot * p.Hv + h;
-                pos0 = p.pos[idx];
-                ck0 = p.ckpt_pos[idx];
-            }
             count = pos0 - ck0;
             if (ck0 < 0 || count < 0 || count > L) {
                 if (lane == 0) set_error(p.dev_err, GDN_DEVERR_RING);
@@ -370,7 +391,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                 const int64_t oi = (((int64_t)b * T + t) * p.Hv + h) * p.dv + j;
                 if (out_ok(oi)) store_elem(p.out, oi, out_dt, 0.f);
             }
-            unit = unit_next;
             continue;
         }
         const int cpr = fold ? 0 : count;  // ring entries in front of the window
@@ -529,12 +549,6 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
                 if (lane == 31) R = ghi, R_hi = 1.f;
                 fsc = lane < count ? R * hdr[lane].z : 0.f;
                 fsc_hi = ring_hi && lane + 32 < count ? R_hi * hdr[lane + 32].z : 0.f;
-                if (slot_n >= 0 && slot_n < p.num_slots) {  // the next unit's pointers
-                    const int64_t ni = (int64_t)slot_n * p.Hv + (unit_next - unit_next / p.Hv * p.Hv);
-                    pos_n = p.pos[ni];
-                    ck_n = p.ckpt_pos[ni];
-                    ptrs_n = true;
-                }
             }
             if (sb == 0 && T > 0) {
 #pragma unroll
@@ -859,7 +873,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_warp_kernel(const ReplayArg
             p.pos[uidx] = pos0 + T;
             if (fold) p.ckpt_pos[uidx] = pos0;
         }
-        unit = unit_next;
+    }
+    __syncthreads();  // the next round rewrites the lists
     }
 }
 
