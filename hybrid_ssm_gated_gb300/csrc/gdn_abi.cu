@@ -128,13 +128,23 @@ int replay_common(const char* fn, int rule, const gdn_dims* dims, const gdn_repl
     p.B = dims->B, p.Hk = dims->Hk, p.Hv = dims->Hv, p.dv = dims->dv, p.L = c->L, p.T = T, p.force = force != 0;
     p.in_dtype = c->ring_dtype, p.out_dtype = T > 0 ? out_dtype : GDN_F32;
     p.q_scale = (float)(1.0 / sqrt((double)dims->dk));
+    // the producer kernel's 16 KB chunks of the read type, and of the master (whose chunk holds a
+    // whole number of the read type's items)
+    if (c->ckpt_read) {
+        chunking(dims->dk, dims->dv, gdn::dtype_size(c->read_dtype), p.rows, p.nchunk);
+        chunking(dims->dk, p.rows, 4, p.mrows, p.mnchunk);
+        p.mnchunk = dims->dv / p.mrows;
+    } else {
+        chunking(dims->dk, dims->dv, gdn::dtype_size(c->ckpt_dtype), p.rows, p.nchunk);
+        p.mrows = p.rows, p.mnchunk = p.nchunk;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int tmax = T <= 1 ? 1 : (T <= 4 ? 4 : 8);
     bool too_big = false;
     cudaError_t e;
     if (c->ckpt_read) {
-        // Two checkpoints, one launch: steps read the copy; folds read the fp32 master, update it
-        // and rewrite the copy.
+        // Two checkpoints, one launch: steps read the copy; folds stream the fp32 master, run the
+        // rule on it, store it and rewrite the copy.
         p.ckpt_copy = c->ckpt_read;
         e = c->read_dtype == GDN_BF16 ? gdn::dispatch_replay_f32_bf16(dims->dk, tmax, p, s, too_big)
                                       : gdn::dispatch_replay_f32_f16(dims->dk, tmax, p, s, too_big);

@@ -7,7 +7,7 @@
 
 #include "gdn_decode.cuh"
 #include "gdn_prefill.cuh"
-#include "gdn_replay_warp.cuh"
+#include "gdn_replay_common.cuh"
 #include "gdn_spec.cuh"
 
 namespace gdn {

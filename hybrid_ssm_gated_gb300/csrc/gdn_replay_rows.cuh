@@ -2,11 +2,10 @@
 // step, the speculative verify window and the fold (flush), one warp per
 // (sequence, value head) unit and one state row per lane.
 //
-// The arithmetic is that of gdn_replay_warp.cuh (AREX article on ReplaySSM,
+// The arithmetic is in gdn_replay_common.cuh (AREX article on ReplaySSM,
 // section "缓存输入而非状态"): outputs from one pass over S0 plus the ring's w
 // terms, the window's own recursion per row, the ring folded into S0 when
-// full. What differs is the layout, which removes every cross-lane reduction
-// from the pass over S0:
+// full. The layout removes every cross-lane reduction from the pass over S0:
 //  - a batch is 64 state rows, lane l owning rows l and 32 + l; the rows
 //    stream through shared memory in 64-byte column chunks (64 rows x 64 B =
 //    4 KB a stage, copied with cp.async by the whole warp, coalesced, into a
@@ -19,16 +18,19 @@
 //    rows; each lane accumulates its rows' 2T dot products (T for Mamba2) in
 //    registers over the chunks, so when a batch's last chunk is done every
 //    lane holds whole row sums and runs the rows' tails at once;
-//  - a fold applies the buffered entries to each chunk as it arrives (raw
-//    keys broadcast from shared memory, the entry's scale and the row's w in
-//    registers), stores it rounded and goes on from the stored value;
+//  - a fold applies the buffered entries to each chunk as it arrives (keys,
+//    normalised once per unit in place, broadcast from shared memory, the
+//    entry's scale and the row's w in registers), stores it rounded and goes
+//    on from the stored value;
 //  - a batch's 64 columns of every buffered entry's w are staged with its
-//    first chunk; a lane reads only the columns of its own rows.
-// The two-checkpoint mode keeps gdn_replay_warp.cuh: its fold runs the rule
-// sequentially on whole master rows, which column chunks do not hold.
+//    first chunk; a lane reads only the columns of its own rows;
+//  - units are taken from per-round lists, fold units first
+//    (gdn_replay_common.cuh).
+// The two-checkpoint mode runs in gdn_replay_producer.cuh: its fold runs the
+// rule sequentially on whole master rows, which column chunks do not hold.
 #pragma once
 
-#include "gdn_replay_warp.cuh"
+#include "gdn_replay_common.cuh"
 
 namespace gdn {
 
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
 #pragma unroll
     for (int m = 0; m < 8; ++m) dso[m] = rows_piece((lane >> 2) + 8 * m, lane & 3);
 
-    // the CTA's units, in rounds of listed units, fold units first (REPLAY_ROUND, gdn_replay_warp.cuh)
+    // the CTA's units, in rounds of listed units, fold units first (REPLAY_ROUND, gdn_replay_common.cuh)
     const int per_cta = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     for (int r0 = 0; r0 < per_cta; r0 += REPLAY_ROUND) {
     const int nr = per_cta - r0 < REPLAY_ROUND ? per_cta - r0 : REPLAY_ROUND;
