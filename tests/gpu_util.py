@@ -43,9 +43,19 @@ def decode_oracle_unit(S: np.ndarray, sdt: str, x: dict, idt: str, b: int, h: in
 
 
 def sample_units(B: int, Hv: int, n: int, seed: int = 123) -> list[tuple[int, int]]:
+    """n (sequence, head) units for a full-size parity run: the first and the last unit, three units of
+    the persistent grid's ragged last round, the rest at random. Every kernel runs one CTA per SM and
+    CTA c takes units c, c + SMs, ...; the units past the last whole round go to only some CTAs, so
+    that round ends the launch unevenly and is where a wrong tail bound would show."""
     r = np.random.default_rng(seed)
+    total = B * Hv
     picks = {(0, 0), (B - 1, Hv - 1)}
-    while len(picks) < min(n, B * Hv):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tail0 = total // sms * sms  # first unit of the ragged round
+    if sms < total and tail0 < total:
+        for u in r.integers(tail0, total, size=3):
+            picks.add(divmod(int(u), Hv))
+    while len(picks) < min(n, total):
         picks.add((int(r.integers(B)), int(r.integers(Hv))))
     return sorted(picks)
 

@@ -291,14 +291,14 @@ def _decode_sampled(name: str, n_units: int):
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mamba2_b256_f32", "mamba2_b256_bf16"])
 def test_decode_b256_sampled(name):
-    _decode_sampled(name, 8)
+    _decode_sampled(name, 16)
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mamba2_replay_b256_f32", "mamba2_replay_b256_bf16"])
 def test_replay_b256_sampled(name):
     w = wl.WORKLOADS[name]
-    H = M2Harness(w, sample_units(w.B, w.Hv, 8, seed=10))
+    H = M2Harness(w, sample_units(w.B, w.Hv, 16, seed=10))
     H.prefill(wl.start_offsets(w))
     for t in range(w.steps):
         H.window(wl.mamba2_step_inputs(w, t), H.slots, 1, f"{name} step {t}")

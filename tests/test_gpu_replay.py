@@ -271,13 +271,13 @@ def _sampled(name: str, n_units: int):
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["replay_b256_f32", "replay_b256_bf16"])
 def test_replay_b256_sampled(name):
-    _sampled(name, 8)
+    _sampled(name, 16)
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["verify_b256_f32", "verify_b256_bf16"])
 def test_verify_b256_sampled(name):
-    _sampled(name, 8)
+    _sampled(name, 16)
 
 
 @pytest.mark.parametrize("rdt", ["bf16", "f16"])
@@ -314,7 +314,7 @@ def test_read_copy_large_head(T):
 @pytest.mark.slow
 def test_read_copy_b256_sampled():
     w = wl.WORKLOADS["replay_b256_f32"]
-    H = Harness(w, sample_units(w.B, w.Hv, 8, seed=6), read_dtype="bf16")
+    H = Harness(w, sample_units(w.B, w.Hv, 16, seed=6), read_dtype="bf16")
     H.prefill(wl.start_offsets(w))
     for r in range(w.steps):
         H.window(wl.step_inputs(w, r), H.slots, 1, f"round {r}")
