@@ -9,13 +9,13 @@
 
 namespace gdn {
 
-// The row-per-lane kernel: its shared memory (22, 25 and 30 KB a warp at L = 16, d = 128, for
-// windows of 1, 4 and 8 tokens) allows 10, 8 and 7 warps. Registers are granted per SM
-// sub-partition, a warp of each four on each, so 13 to 16 warps leave 128 registers a thread, 9 to 12
-// leave 168 and 5 to 8 leave 255: compiled for 16, 8 and 8.
+// The row-per-lane kernel: its shared memory (18, 21 and 26 KB a warp at L = 16, d = 128 with bf16
+// activations, for windows of 1, 4 and 8 tokens) allows 12, 10 and 8 warps. Registers are granted
+// per SM sub-partition, a warp of each four on each, so 13 to 16 warps leave 128 registers a thread,
+// 9 to 12 leave 168 and 5 to 8 leave 255: compiled for 16, 12 and 8.
 template <int TMAX>
 constexpr int replay_rows_warps() {
-    return TMAX == 1 ? 16 : 8;
+    return TMAX == 1 ? 16 : (TMAX <= 4 ? 12 : 8);
 }
 
 // The two-checkpoint warp kernel (the producer kernel's fallback): warps by window size. The kernel

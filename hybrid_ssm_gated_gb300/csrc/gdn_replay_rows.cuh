@@ -18,10 +18,10 @@
 //    rows; each lane accumulates its rows' 2T dot products (T for Mamba2) in
 //    registers over the chunks, so when a batch's last chunk is done every
 //    lane holds whole row sums and runs the rows' tails at once;
-//  - a fold applies the buffered entries to each chunk as it arrives (keys,
-//    normalised once per unit in place, broadcast from shared memory, the
-//    entry's scale and the row's w in registers), stores it rounded and goes
-//    on from the stored value;
+//  - a fold applies the buffered entries to each chunk as it arrives (raw
+//    keys broadcast from shared memory, the entry's scale -- decay and 1/|k| --
+//    and the row's w in registers), stores it rounded and goes on from the
+//    stored value;
 //  - a batch's 64 columns of every buffered entry's w are staged with its
 //    first chunk; a lane reads only the columns of its own rows;
 //  - units are taken from per-round lists, fold units first
@@ -49,8 +49,8 @@ struct RowsCfg {
 };
 
 // One warp's shared memory: the copy stages; the window's normalised keys and queries [TMAX][DK]
-// each; the buffered keys [L][DK], normalised fp32 (staged raw at the end of their region and
-// converted in place), and record headers {alpha, beta, 1/|k|, n} [L]; the current
+// each; the buffered keys [L][DK] as stored (raw, in the activation dtype: their 1/|k| joins the
+// scalars they are multiplied by), and record headers {alpha, beta, 1/|k|, n} [L]; the current
 // batch's 64 columns of every buffered entry's w [L][64]; the coefficient table [L + TMAX][CW].
 struct RowsLayout {
     int stage, kwin, qwin, keys, hdr, wcol, coef, bytes;
@@ -64,7 +64,7 @@ __host__ __device__ constexpr RowsLayout replay_rows_layout(int L, int in_sz) {
     w.kwin = C::NS * C::STAGE;
     w.qwin = w.kwin + TMAX * DK * 4;
     w.keys = w.qwin + TMAX * DK * 4;
-    w.hdr = w.keys + L * DK * 4;
+    w.hdr = w.keys + L * DK * in_sz;
     w.wcol = w.hdr + L * 16;
     w.coef = w.wcol + L * 64 * 4;
     w.bytes = align_up(w.coef + (L + TMAX) * C::CW * 4, 16);
@@ -115,9 +115,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
     unsigned char* stages = region + lay.stage;
     float* kwin = reinterpret_cast<float*>(region + lay.kwin);  // [TMAX][DK] normalised window keys
     float* qwin = reinterpret_cast<float*>(region + lay.qwin);  // [TMAX][DK] normalised, scaled queries
-    unsigned char* keys = region + lay.keys;                    // [L][DK] buffered keys
-    float* keysf = reinterpret_cast<float*>(keys);               // ... normalised, once converted
-    const int rawoff = p.L * DK * 4 - p.L * DK * in_sz;          // where the raw keys are staged
+    unsigned char* keys = region + lay.keys;                    // [L][DK] buffered keys, raw
     const float4* hdr = reinterpret_cast<const float4*>(region + lay.hdr);
     float* wcol = reinterpret_cast<float*>(region + lay.wcol);  // [L][64] w of the batch's columns
     float* coef = reinterpret_cast<float*>(region + lay.coef);  // [entry][CW]: S^T k at [t], S^T q at [TMAX + t]
@@ -252,7 +250,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                         const unsigned char* src =
                             static_cast<const unsigned char*>(p.ring_k) + (unit_ring + ring_at(f)) * kbytes + k * 16;
                         if (in_bounds(src, 16, p.ring_k, ext_rk, p.dev_err))
-                            cp_async_piece<16>(keys + rawoff + f * kbytes + k * 16, src);
+                            cp_async_piece<16>(keys + f * kbytes + k * 16, src);
                     }
                     issue_w(0);
                 }
@@ -317,7 +315,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         cp_async_wait<NS - 2>();
         __syncwarp();
         // ring decays by suffix products over the staged alphas: R(f) = prod_{f<g<count} alpha_g
-        // (lane f; entries 32 + f in the _hi values), their product, a fold's R(f) / |k_f|
+        // (lane f; entries 32 + f in the _hi values), their product, and a fold's scale of the raw key
+        // k_f, R(f) / |k_f|
         float suf = lane < count ? hdr[lane].x : 1.f;
         float suf_hi = ring_hi && lane + 32 < count ? hdr[lane + 32].x : 1.f;
 #pragma unroll
@@ -335,21 +334,8 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         R = __shfl_down_sync(FULL_MASK, suf, 1);
         R_hi = ring_hi ? __shfl_down_sync(FULL_MASK, suf_hi, 1) : 1.f;
         if (lane == 31) R = ghi, R_hi = 1.f;
-        fsc = lane < count ? R : 0.f;
-        fsc_hi = ring_hi && lane + 32 < count ? R_hi : 0.f;
-        // the buffered keys to normalised fp32, in entry order: the fp32 row of entry f overlaps only the
-        // raw rows of entries up to f, so each entry's raw elements are read (by all lanes) before its
-        // fp32 row is written
-        for (int f = 0; f < count; ++f) {
-            const float ik = hdr[f].z;
-            float kv[EPL];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) kv[e] = load_elem(keys + rawoff + f * kbytes, lane * EPL + e, in_dt) * ik;
-            __syncwarp();
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) keysf[f * DK + lane * EPL + e] = kv[e];
-        }
-        __syncwarp();
+        fsc = lane < count ? R * hdr[lane].z : 0.f;
+        fsc_hi = ring_hi && lane + 32 < count ? R_hi * hdr[lane + 32].z : 0.f;
         if (T > 0) {
             // ------------------------------ coefficient table
             // entry x (ring entry f = x < cpr, else window token s = x - cpr) against every window
@@ -370,8 +356,17 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     const int x = x0 + i < J ? x0 + i : J - 1;
                     float kx[EPL];
                     if (x < cpr) {
+                        // the raw key, normalised here
+                        const float ik = hdr[x].z;
+                        if constexpr (EPL % 4 == 0) {
 #pragma unroll
-                        for (int e = 0; e < EPL; ++e) kx[e] = keysf[x * DK + lane * EPL + e];
+                            for (int e = 0; e < EPL; e += 4) load_run<4>(keys + x * kbytes, lane * EPL + e, in_dt, kx + e);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < EPL; ++e) kx[e] = load_elem(keys + x * kbytes, lane * EPL + e, in_dt);
+                        }
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) kx[e] *= ik;
                     } else {
 #pragma unroll
                         for (int e = 0; e < EPL; ++e) kx[e] = kwin[(x - cpr) * DK + lane * EPL + e];
@@ -479,8 +474,9 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                     const float2 w1 = make_float2(w1s, w1s);
 #pragma unroll
                     for (int g4 = 0; g4 < CE / 4; ++g4) {
-                        const float4 kf = *reinterpret_cast<const float4*>(keysf + f * DK + e0 + 4 * g4);
-                        const float2 k01 = make_float2(kf.x, kf.y), k23 = make_float2(kf.z, kf.w);
+                        float kf[4];  // the raw key's elements (its 1/|k| is in the scale)
+                        load_run<4>(keys + f * kbytes, e0 + 4 * g4, in_dt, kf);
+                        const float2 k01 = make_float2(kf[0], kf[1]), k23 = make_float2(kf[2], kf[3]);
                         float2 a = make_float2(s[0][4 * g4], s[0][4 * g4 + 1]), c = make_float2(s[0][4 * g4 + 2], s[0][4 * g4 + 3]);
                         a = __ffma2_rn(k01, w0, a), c = __ffma2_rn(k23, w0, c);
                         s[0][4 * g4] = a.x, s[0][4 * g4 + 1] = a.y, s[0][4 * g4 + 2] = c.x, s[0][4 * g4 + 3] = c.y;
