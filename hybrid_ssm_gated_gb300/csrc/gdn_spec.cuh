@@ -7,7 +7,7 @@
 // verification the state of the last accepted token is already stored; the
 // recursion itself continues in FP32 registers. It costs one state read and
 // T state writes per sequence and head, where the ReplaySSM verify window
-// (gdn_replay.cuh) reads the checkpoint once and writes no state: this kernel
+// (gdn_replay_rows.cuh) reads the checkpoint once and writes no state: this kernel
 // is the comparison point for that claim. The AREX article on ReplaySSM
 // describes the baseline in its section "每步写回完整循环状态：SSM 解码的两个
 // 瓶颈" (a recurrent state kept per draft token, about (1 + num_spec) times
