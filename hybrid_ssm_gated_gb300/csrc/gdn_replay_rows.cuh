@@ -17,7 +17,12 @@
 //    read as broadcasts, four elements at a time, shared by the lane's two
 //    rows; each lane accumulates its rows' 2T dot products (T for Mamba2) in
 //    registers over the chunks, so when a batch's last chunk is done every
-//    lane holds whole row sums and runs the rows' tails at once;
+//    lane holds whole row sums and runs the rows' tails at once. Windows of 4
+//    and 8 tokens over a 16-bit checkpoint take these dot products on the
+//    tensor cores instead (warp-level TF32 MMA, the checkpoint exact in TF32,
+//    the vectors split hi + lo), and turn the fragments into row sums through
+//    the stage at a batch's end (measured: bf16 windows of four 195 -> 185 us
+//    at B = 256; an FP32 checkpoint, needing three products, was slower);
 //  - a fold applies the buffered entries to each chunk as it arrives (raw
 //    keys broadcast from shared memory, the entry's scale -- decay and 1/|k| --
 //    and the row's w in registers), stores it rounded and goes on from the
@@ -95,6 +100,28 @@ __device__ __forceinline__ void ld4(const unsigned char* src, float* x) {
     }
 }
 
+// x as a TF32 pair hi + lo, each rounded to nearest: hi keeps the top 11 significand bits, lo the next
+// 11, so that hi b + lo b and hi b' products keep FP32-level accuracy.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+// d += a b on the tensor cores, one warp: a 16 x 8 (row fragment), b 8 x 8 (column fragment), d 16 x 8,
+// TF32 operands, FP32 accumulation (PTX ISA, mma.m16n8k8 fragment layouts for .tf32).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <typename ST, int DK, int TMAX, int NW, int RULE = RULE_GDN, int IO = IO_ANY>
 __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArgs p) {
     using C = RowsCfg<ST, DK, TMAX, RULE>;
@@ -102,6 +129,12 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
     constexpr int SZ = C::SZ, CE = C::CE, NCH = C::NCH, NS = C::NS;
     constexpr int SROW = DK * SZ;
     constexpr int EPL = DK / 32;  // key elements per lane in the warp-wide dot products
+    // windows of 4 and 8 tokens over a 16-bit checkpoint take the pass's dot products on the tensor
+    // cores (MMA_NT tiles of 8 window vectors); single tokens (2 sums a row, Mamba2 1) and FP32
+    // checkpoints (whose TF32 split needs three products) measured faster on the FMA pipe
+    constexpr bool MMA = TMAX >= 4 && sizeof(ST) == 2;
+    constexpr int MMA_NT = (C::VPR + 7) / 8;
+    constexpr int KS = CE / 8;  // k-steps of 8 in a chunk
     const int in_dt = io_in<IO>(p.in_dtype), out_dt = io_out<IO>(p.out_dtype);
     const int in_sz = dtype_size(in_dt);
     // dynamic shared memory: the round's counters and unit lists, then one region per warp
@@ -309,6 +342,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
         const int64_t out_b = ((int64_t)b * T * p.Hv + h) * p.dv;  // output (t = 0, j = 0)
         const int64_t out_t = (int64_t)p.Hv * p.dv;                // next token
         float2 acc[2][C::VPR];  // the lane's two rows' partial sums: S0^T k_t at [t], S0^T q_t at [NK - 1 ...]
+        float dm[4][MMA ? MMA_NT : 1][4];  // tensor-core sums: m-tile (16 rows), n-tile, fragment
         float vx_pre[2][TMAX];  // the window's values at the lane's two columns of the current batch
 
         // the unit's first stage, with the buffered keys and headers
@@ -434,6 +468,12 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
                     for (int v = 0; v < C::VPR; ++v) acc[r][v] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < (MMA ? MMA_NT : 1); ++nt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dm[mt][nt][i] = 0.f;
                 if (T > 0) {
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
@@ -494,7 +534,16 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                         if (in_bounds(dst + (e0 + v) * SZ, 16, p.ckpt, ext_ckpt, p.dev_err))
                             st_state<ST, 16 / SZ>(dst, e0 + v, s[r] + v);
                 }
-                if (T > 0) {
+                if (MMA && T > 0) {
+                    // the stored (rounded) rows back into the stage, where the tensor-core pass reads them
+                    unsigned char* st = stages + (q % NS) * C::STAGE;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int pc = 0; pc < 4; ++pc)
+                            *reinterpret_cast<uint4*>(st + rows_piece(32 * r + lane, pc)) =
+                                Store<ST>::pack(s[r] + pc * (16 / SZ));
+                } else if (T > 0) {
 #pragma unroll
                     for (int g4 = 0; g4 < CE / 4; ++g4) {
 #pragma unroll
@@ -521,7 +570,7 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                         }
                     }
                 }
-            } else if (T > 0) {
+            } else if (!MMA && T > 0) {
                 // the lane's rows' dot products with the window's keys and queries, four elements at a time
 #pragma unroll
                 for (int g4 = 0; g4 < CE / 4; ++g4) {
@@ -551,6 +600,79 @@ __global__ void __launch_bounds__(NW * 32, 1) replay_rows_kernel(const ReplayArg
                             }
                         }
                     }
+                }
+            }
+            if (MMA && T > 0) {
+                // The chunk's rows against the window's vectors on the tensor cores: D[row][n] +=
+                // S0[row][.] . vec_n[.], rows as M (4 tiles of 16), the chunk's CE columns as K, vector n
+                // (GDN: keys of tokens 0..TMAX-1, then queries; Mamba2: queries) as N. The columns are
+                // permuted within the chunk so that a lane's A and B elements are one 16-byte piece: lane
+                // (g, c) takes columns (CE / 4) c + 2 s and + 1 as its k = c and c + 4 of k-step s.
+                // 16-bit checkpoint values are exact in TF32; the vectors are split into TF32 hi + lo.
+                if (fold) __syncwarp();  // every lane's folded rows are in the stage
+                const int g = lane >> 2, c = lane & 3;
+                const int rows = p.dv - j0 < 64 ? p.dv - j0 : 64;
+                uint32_t bh[MMA ? MMA_NT : 1][2 * KS], bl[MMA ? MMA_NT : 1][2 * KS];
+#pragma unroll
+                for (int nt = 0; nt < (MMA ? MMA_NT : 1); ++nt) {
+                    const int n = 8 * nt + g;
+                    float bv[2 * KS];
+#pragma unroll
+                    for (int i = 0; i < 2 * KS; i += 4) {
+                        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (n < C::VPR)
+                            f = *reinterpret_cast<const float4*>((GDN ? kwin : qwin) + n * DK + e0 + (CE / 4) * c + i);
+                        bv[i] = f.x, bv[i + 1] = f.y, bv[i + 2] = f.z, bv[i + 3] = f.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2 * KS; ++i) split_tf32(bv[i], bh[nt][i], bl[nt][i]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    if (16 * mt >= rows) break;
+                    float a0[2 * KS], a1[2 * KS];  // rows 16 mt + g and + 8, the lane's piece
+                    Store<ST>::unpack(*reinterpret_cast<const uint4*>(stg + rows_piece(16 * mt + g, c)), a0);
+                    Store<ST>::unpack(*reinterpret_cast<const uint4*>(stg + rows_piece(16 * mt + g + 8, c)), a1);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const uint32_t x0 = __float_as_uint(a0[2 * ks]), x1 = __float_as_uint(a1[2 * ks]);
+                        const uint32_t x2 = __float_as_uint(a0[2 * ks + 1]), x3 = __float_as_uint(a1[2 * ks + 1]);
+#pragma unroll
+                        for (int nt = 0; nt < (MMA ? MMA_NT : 1); ++nt) {
+                            mma_tf32(dm[mt][nt], x0, x1, x2, x3, bl[nt][2 * ks], bl[nt][2 * ks + 1]);
+                            mma_tf32(dm[mt][nt], x0, x1, x2, x3, bh[nt][2 * ks], bh[nt][2 * ks + 1]);
+                        }
+                    }
+                }
+                if (ch == NCH - 1) {
+                    // the batch's sums from the fragments (lane (g, c): rows g and g + 8 of each m-tile,
+                    // vectors 2c and 2c + 1 of each n-tile) to the row layout (lane l: rows l and 32 + l,
+                    // every vector) through the stage, which the pass no longer reads
+                    __syncwarp();
+                    unsigned char* scr = stages + (q % NS) * C::STAGE;
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        if (16 * mt >= rows) break;
+#pragma unroll
+                        for (int nt = 0; nt < (MMA ? MMA_NT : 1); ++nt)
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int n = 8 * nt + 2 * c;
+                                *reinterpret_cast<float2*>(scr + rows_piece(16 * mt + g + 8 * hh, n >> 2) + (n & 3) * 4) =
+                                    make_float2(dm[mt][nt][2 * hh], dm[mt][nt][2 * hh + 1]);
+                            }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int pc = 0; pc < (C::VPR + 3) / 4; ++pc) {
+                            const float4 f = *reinterpret_cast<const float4*>(scr + rows_piece(32 * r + lane, pc));
+                            const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (4 * pc + i < C::VPR) acc[r][4 * pc + i] = make_float2(fv[i], 0.f);
+                        }
                 }
             }
             if (ch != NCH - 1) continue;
