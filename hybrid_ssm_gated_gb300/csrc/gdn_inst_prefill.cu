@@ -2,6 +2,7 @@
 #include "gdn_dispatch.h"
 #include "gdn_launch.cuh"
 #include "gdn_prefill.cuh"
+#include "gdn_prefill_tc.cuh"
 
 namespace gdn {
 
@@ -25,10 +26,31 @@ cudaError_t launch_prefill(PrefillArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// The bf16-in / fp32-out instantiation when the arguments match it, the generic one otherwise.
+// The chunked tensor-core prefill: one CTA per (sequence, value head, 128 state rows).
+template <typename ST, int IO>
+cudaError_t launch_prefill_tc(PrefillArgs& a, cudaStream_t stream) {
+    auto kern = prefill_tc_kernel<ST, IO>;
+    int bps = 0;
+    cudaError_t e = prepare_kernel(kern, tc::THREADS, tc::SMEM, bps);
+    if (e != cudaSuccess) return e;
+    a.row_blocks = a.dv / tc::ROWS;
+    const int64_t grid = (int64_t)a.B * a.Hv * a.row_blocks;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, tc::THREADS, tc::SMEM, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// The bf16-in / fp32-out instantiation when the arguments match it, the generic one otherwise. 16-bit
+// states with dk = 128 and dv a multiple of 128 take the chunked tensor-core kernel; FP32 states (whose
+// tolerance one TF32 pass does not meet) and other shapes the sequential one.
 template <typename ST, int DK>
 cudaError_t launch_prefill_io(PrefillArgs& a, cudaStream_t stream) {
-    if (io_mode(a.in_dtype, a.out_dtype) == IO_BF16_F32) return launch_prefill<ST, DK, IO_BF16_F32>(a, stream);
+    const bool bf16_f32 = io_mode(a.in_dtype, a.out_dtype) == IO_BF16_F32;
+    if constexpr (sizeof(ST) == 2 && DK == tc::DKT) {
+        if (a.dv % tc::ROWS == 0)
+            return bf16_f32 ? launch_prefill_tc<ST, IO_BF16_F32>(a, stream) : launch_prefill_tc<ST, IO_ANY>(a, stream);
+    }
+    if (bf16_f32) return launch_prefill<ST, DK, IO_BF16_F32>(a, stream);
     return launch_prefill<ST, DK, IO_ANY>(a, stream);
 }
 

@@ -83,10 +83,11 @@ def test_prefill_other_head_shapes(dk, dv, Hk, Hv, sdt):
     _check_all(w, [3, 16, 40, 0], wl.slots(w), 8)
 
 
-@pytest.mark.parametrize("sdt", ["f32", "bf16"])
-def test_prefill_extreme_decays(sdt):
-    # decays near 1, tiny ones and ones that underflow FP32 (A_log = 5, dt_bias = 5: alpha ~ e^-740)
-    w = wl.Workload("pfx", B=3, Hk=1, Hv=4, dk=64, dv=64, steps=1, state_dtype=sdt, in_dtype="f32", seed=66)
+@pytest.mark.parametrize("sdt,d", [("f32", 64), ("bf16", 64), ("bf16", 128), ("f16", 128)])
+def test_prefill_extreme_decays(sdt, d):
+    # decays near 1, tiny ones and ones that underflow FP32 (A_log = 5, dt_bias = 5: alpha ~ e^-740); with
+    # 16-bit states and d = 128 on the chunked tensor-core kernel, whose decays are ratios within a chunk
+    w = wl.Workload("pfx", B=3, Hk=1, Hv=4, dk=d, dv=d, steps=1, state_dtype=sdt, in_dtype="f32", seed=66)
     params = (np.array([-4.0, 1.0, 3.0, 5.0], np.float32), np.array([-6.0, 0.0, 2.0, 5.0], np.float32))
     _check_all(w, [40, 70, 17], wl.slots(w), 16, params=params)
 
