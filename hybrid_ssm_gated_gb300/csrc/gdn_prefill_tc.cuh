@@ -35,8 +35,9 @@
 //  4. tcgen05 MMAs: delta^T P^T (the outputs' intra-chunk part) and delta^T K~
 //     (the state update);
 //  5. outputs and the new state (rounded at a rounding point) by the threads.
-// Operands are TF32 (FP32 storage rounded to TF32 when written); accumulation
-// is FP32. One TF32 pass keeps 16-bit states within their own rounding (in an
+// Operands are FP32 values in shared memory of which the MMA (kind::tf32)
+// takes the TF32 part; accumulation is FP32 (rounding the operands to TF32
+// first measured 4% slower, with the same parity). One TF32 pass keeps 16-bit states within their own rounding (in an
 // emulation of this form over 2048-token sequences: state max-abs 2.2e-3 with a
 // bf16 state, outputs 4.7e-5); FP32 states stay on prefill_kernel.
 //
@@ -70,8 +71,8 @@ constexpr int OFF_A = OFF_D + 128 * 64 * 4;    // A: [64 t][68] row-major (padde
 constexpr int A_LD = 68;
 constexpr int OFF_P = OFF_A + 64 * A_LD * 4;   // P: [64 t][64 s], operand layout
 constexpr int OFF_KT = OFF_P + 64 * 64 * 4;    // K~: [128 i][64 s], operand layout
-constexpr int OFF_G = OFF_KT + 128 * 64 * 4;   // g[64], beta[64]
-constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;    // mbarrier, TMEM address
+constexpr int OFF_G = OFF_KT + 128 * 64 * 4;   // per token: g, beta, 2^g, alpha, 2^(g_C - g) [5][64]
+constexpr int OFF_BAR = OFF_G + 5 * 64 * 4;    // mbarrier, TMEM address
 constexpr int SMEM = OFF_BAR + 16;
 static_assert(SMEM <= 232448, "shared memory");
 // TMEM columns
@@ -182,11 +183,6 @@ __device__ __forceinline__ float ex2(float x) {
     return r;
 }
 
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
 
 }  // namespace tc
 
@@ -232,8 +228,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
     float* sA = reinterpret_cast<float*>(smem + OFF_A);
     unsigned char* sP = smem + OFF_P;
     unsigned char* sKT = smem + OFF_KT;
-    float* sg = reinterpret_cast<float*>(smem + OFF_G);  // g[64], then beta[64]
-    float* sbeta = sg + 64;
+    float* sg = reinterpret_cast<float*>(smem + OFF_G);  // cumulative base-2 log-decay g_t (inclusive)
+    float* sbeta = sg + 64;                              // beta_t
+    float* seg = sg + 128;                               // 2^{g_t}
+    float* salpha = sg + 192;                            // alpha_t = 2^{g_t - g_{t-1}}
+    float* skt = sg + 256;                               // 2^{g_C - g_t}
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8);
     unsigned char* gstate =
@@ -370,6 +369,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                 la[hf] = live ? eA * sp : 0.f;
                 be[hf] = live ? 1.f / (1.f + expf(-gate_in(gr[hf][1]))) : 0.f;
             }
+            const float step[2] = {la[0], la[1]};  // each token's own log-decay
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -378,11 +378,15 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                     if (lane >= off) la[hf] += o;
                 }
             la[1] += __shfl_sync(FULL_MASK, la[0], 31);
-            sg[lane] = la[0], sg[32 + lane] = la[1];
-            sbeta[lane] = be[0], sbeta[32 + lane] = be[1];
+            const float gc = __shfl_sync(FULL_MASK, (C - 1) >> 5 ? la[1] : la[0], (C - 1) & 31);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int t = lane + 32 * hf;
+                sg[t] = la[hf], sbeta[t] = be[hf];
+                seg[t] = ex2(la[hf]), salpha[t] = ex2(step[hf]), skt[t] = ex2(gc - la[hf]);
+            }
         }
         __syncthreads();
-        const float gC = sg[C - 1];
 
         // ---- 1b. [K; Q] normalised (rows n < 64 keys, 64 + t queries), K~ = 2^{g_C - g_s} k_s transposed
 #pragma unroll
@@ -410,16 +414,35 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
             ss += __shfl_xor_sync(FULL_MASK, ss, 16);
             const float sc = rsqrtf(ss + 1e-6f) * (key ? 1.f : p.q_scale);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[grp][e] = to_tf32(x[grp][e] * sc);
+            for (int e = 0; e < 32; ++e) x[grp][e] = (x[grp][e] * sc);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<float4*>(sKQ + op_off(n, 32 * qq + 4 * c, 128)) =
                     make_float4(x[grp][4 * c], x[grp][4 * c + 1], x[grp][4 * c + 2], x[grp][4 * c + 3]);
             if (key) {
-                const float dk = t < C ? ex2(gC - sg[t]) : 0.f;
+                // K~ element (i, t): store k of the lane writes element e = 8 (k / 8) + ((k ^ key3) & 7), key3
+                // = 2 qq + rr / 4, so that the 32 lanes of a store hit 32 banks (bank: (e & 7) 4 + t & 3). The
+                // lane's registers are first permuted by XOR with key3 within groups of 8 (three conditional
+                // swap stages), so that store k reads register k.
+                const float dk = t < C ? skt[t] : 0.f;
+                const int key3 = (2 * qq + (rr >> 2)) & 7;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    *reinterpret_cast<float*>(sKT + op_off(32 * qq + e, t, 128)) = to_tf32(x[grp][e] * dk);
+                for (int e = 0; e < 32; ++e) x[grp][e] = (x[grp][e] * dk);
+#pragma unroll
+                for (int bit = 1; bit < 8; bit <<= 1) {
+                    const bool sw = key3 & bit;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (!(e & bit)) {
+                            const float a0 = x[grp][e], a1 = x[grp][e | bit];
+                            x[grp][e] = sw ? a1 : a0, x[grp][e | bit] = sw ? a0 : a1;
+                        }
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int e = (k & ~7) | ((k ^ key3) & 7);
+                    *reinterpret_cast<float*>(sKT + op_off(32 * qq + e, t, 128)) = x[grp][k];
+                }
             }
         }
         cp_async_wait<0>();  // this thread's value pieces (visible to all after the barrier below)
@@ -456,12 +479,15 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                 const int n = 32 * (warp & 3) + lane;
                 const bool key = n < 64;
                 const int t = key ? n : n - 64;
-                const float gt = sg[t], bt = key ? sbeta[t] : 1.f;
+                const float bt = key ? sbeta[t] : 1.f;
                 tmem_ld<64>(tmem + lane_base + C_G, v);
+                // 2^{g_t - g_s} = alpha_{s+1} ... alpha_t, built downwards from s = t
+                float f = 1.f;
 #pragma unroll
-                for (int s_ = 0; s_ < CH; ++s_) {
-                    const float e = bt * ex2(gt - sg[s_]) * v[s_];
-                    v[s_] = key ? (s_ < t ? e : 0.f) : to_tf32(s_ <= t ? e : 0.f);
+                for (int s_ = CH - 1; s_ >= 0; --s_) {
+                    f = s_ >= t ? 1.f : f * salpha[s_ + 1];
+                    const float e = bt * f * v[s_];
+                    v[s_] = key ? (s_ < t ? e : 0.f) : (s_ <= t ? e : 0.f);
                 }
                 if (key) {
 #pragma unroll
@@ -477,7 +503,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                 tmem_ld<64>(tmem + lane_base + C_SKQ, v);
 #pragma unroll
                 for (int s_ = 0; s_ < CH; ++s_)
-                    v[s_] = to_tf32(s_ < C ? load_elem(sD + s_ * ROWS * isz, j, in_dt) - ex2(sg[s_]) * v[s_] : 0.f);
+                    v[s_] = (s_ < C ? load_elem(sD + s_ * ROWS * isz, j, in_dt) - seg[s_] * v[s_] : 0.f);
 #pragma unroll
                 for (int i = 0; i < CH; i += 4)
                     *reinterpret_cast<float4*>(sY + op_off(j, i, 128)) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
@@ -545,10 +571,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
         for (int o = tid; o < 64 * 16; o += THREADS) {
             const int t = o >> 4, s4 = (o & 15) * 4;
             float4 v = *reinterpret_cast<const float4*>(sTi + t * 64 + s4);
-            v.x = s4 + 0 <= t ? to_tf32(v.x * sbeta[s4 + 0]) : 0.f;
-            v.y = s4 + 1 <= t ? to_tf32(v.y * sbeta[s4 + 1]) : 0.f;
-            v.z = s4 + 2 <= t ? to_tf32(v.z * sbeta[s4 + 2]) : 0.f;
-            v.w = s4 + 3 <= t ? to_tf32(v.w * sbeta[s4 + 3]) : 0.f;
+            v.x = s4 + 0 <= t ? (v.x * sbeta[s4 + 0]) : 0.f;
+            v.y = s4 + 1 <= t ? (v.y * sbeta[s4 + 1]) : 0.f;
+            v.z = s4 + 2 <= t ? (v.z * sbeta[s4 + 2]) : 0.f;
+            v.w = s4 + 3 <= t ? (v.w * sbeta[s4 + 3]) : 0.f;
             *reinterpret_cast<float4*>(sT + op_off(t, s4, 64)) = v;
         }
         fence_async_smem();
@@ -571,7 +597,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4*>(sD + op_off(j, tb + i, 128)) =
-                    make_float4(to_tf32(v[i]), to_tf32(v[i + 1]), to_tf32(v[i + 2]), to_tf32(v[i + 3]));
+                    make_float4(v[i], (v[i + 1]), (v[i + 2]), (v[i + 3]));
         }
         fence_async_smem();
         fence_before();
@@ -603,14 +629,14 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                 for (int i = 0; i < 32; ++i) {
                     const int t = tb + i;
                     if (t < C) {
-                        const float o = fmaf(ex2(sg[t]), sq[i], oi[i]);
+                        const float o = fmaf(seg[t], sq[i], oi[i]);
                         const int64_t idx = ((tok0 + t) * p.Hv + h) * p.dv + row0 + j;
                         if (in_bounds(static_cast<char*>(p.out) + idx * osz, osz, p.out, ext_out, p.dev_err))
                             store_elem(p.out, idx, out_dt, o);
                     }
                 }
             }
-            const float eg = ex2(gC);
+            const float eg = seg[C - 1];
             const bool last = c0 + C == T;
             const int i0 = 64 * hw;
             float u[64];
