@@ -38,6 +38,7 @@ L_RING, T_VERIFY = 16, 4
 # Mamba2 layer: groups, heads, state dim, head dim
 M2_G, M2_H, M2_N, M2_P = 8, 128, 128, 64
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0  # dense bf16 burst, one earlier measurement on a GB300
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, ~8 TB/s nominal
 KERNEL_SOURCES = ["gdn_decode.cuh", "gdn_device.cuh", "gdn_launch.cuh"]
 
@@ -522,8 +523,11 @@ def fp32_alu_peak_tflops(dev) -> tuple[float, str]:
 
 def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
     """Prefill of 19 sequences of 2048 tokens (Hk=16, Hv=32, dk=dv=128, bf16 activations), state written
-    back every 64 tokens, fp32 and bf16 state: tokens/s and the FP32 rate of the rule's 7 dk dv flops per
-    token and head against the FP32 FMA peak. Returns the number of timed launches."""
+    back every 64 tokens, fp32 and bf16 state: tokens/s. The fp32 state runs the sequential kernel: its rate
+    is the rule's 7 dk dv flops per token and head against the FP32 FMA peak. The bf16 state runs the
+    chunked kernel on the tcgen05 tensor cores (TF32 operands): its rate is the MMA flops per launch against
+    a TF32 peak, the measured bf16 GEMM rate times the nominal dense TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s),
+    with its HBM fraction beside it. Returns the number of timed launches."""
     import numpy as np
     import torch
 
@@ -541,17 +545,42 @@ def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
     out = torch.empty(total, w.Hv, w.dv, device=dev)
     peak, peak_note = fp32_alu_peak_tflops(dev)
     flops = 7 * w.dk * w.dv * w.Hv * total
+    # the chunked kernel's MMAs per chunk of 64 tokens and 128 state rows: S0 [K;Q]^T (128x128x128), [K;Q] K^T
+    # (128x64x128), Y T^T and delta^T P^T (128x64x64 each), delta^T K~ (128x128x64)
+    chunks = w.B * w.Hv * (w.dv // 128) * ((w.prefill_len + 63) // 64)
+    mma_flops = chunks * 2 * (128 * 128 * 128 + 128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+    bf16_peak, bf16_note = 0.0, "MEASURED_PEAKS.json absent"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak, bf16_note = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        bf16_peak, bf16_note = FALLBACK_BF16_TFLOPS, "fallback"
+    tf32_peak = bf16_peak * 1.1 / 2.25
+    hbm_peak, _, _ = load_peaks()
+    in_b = 2
+    hbm_bytes = total * (2 * w.Hk * w.dk * in_b + w.Hv * w.dv * in_b + 2 * w.Hv * in_b + w.Hv * w.dv * 4)
     calls = max(5, args.steps // 200)
     for name, sdt in (("fp32", torch.float32), ("bf16", torch.bfloat16)):
         pool = (torch.randn(w.num_slots, w.Hv, w.dv, w.dk, generator=gen, device=dev) * 0.1).to(sdt)
         el, lm = timed(lambda: gdn.gdn_prefill(pool, slots, cu, q, k, v, a, b, A_log, dt_bias, out, err, 64, stream),
                        calls, 3)
-        tf = flops / (lm / 1e3) / 1e12
-        modes[f"prefill_{name}_state"] = {
-            "tokens_per_s": world * total * calls / (el / 1e3), "us_per_call": el / calls * 1e3,
-            "sequences": w.B, "tokens_per_sequence": w.prefill_len, "state_write_interval": 64,
-            "bound": "alu", "alu_tflops": tf, "alu_peak_tflops": peak, "frac": tf / peak, "peak_derivation": peak_note,
-            "flops_per_token": flops / total}
+        entry = {"tokens_per_s": world * total * calls / (el / 1e3), "us_per_call": el / calls * 1e3,
+                 "sequences": w.B, "tokens_per_sequence": w.prefill_len, "state_write_interval": 64}
+        state_bytes = 2 * w.B * w.Hv * w.dv * w.dk * pool.element_size()
+        gbs = (hbm_bytes + state_bytes) / (lm / 1e3) / 1e9
+        if name == "fp32":
+            tf = flops / (lm / 1e3) / 1e12
+            entry.update({"kernel": "prefill_kernel (sequential, FP32 FMA)", "bound": "alu", "alu_tflops": tf,
+                          "alu_peak_tflops": peak, "frac": tf / peak, "peak_derivation": peak_note,
+                          "flops_per_token": flops / total})
+        else:
+            tf = mma_flops / (lm / 1e3) / 1e12
+            entry.update({"kernel": "prefill_tc_kernel (chunked, tcgen05 TF32)", "bound": "tensor",
+                          "tensor_tflops": tf, "tf32_peak_tflops": tf32_peak, "frac": tf / tf32_peak,
+                          "peak_derivation": f"{bf16_note} bf16 {bf16_peak:.0f} TFLOP/s x 1.1 / 2.25",
+                          "mma_flops_per_launch": mma_flops})
+        entry.update({"hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak})
+        modes[f"prefill_{name}_state"] = entry
         del pool
     return 2 * calls
 

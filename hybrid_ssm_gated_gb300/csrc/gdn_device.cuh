@@ -91,11 +91,6 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Prefetch `bytes` (a multiple of 16) at `g` (16-byte aligned) into L2: a hint, nothing to wait for.
-__device__ __forceinline__ void prefetch_l2(const void* g, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
-}
-
 // L2 policy for data read once (state tiles): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -264,6 +264,10 @@ int gdn_rollback(const gdn_dims* dims, const gdn_replay_cache* cache, const int3
  * rounded to state_dtype after every state_write_interval tokens (the next
  * chunk continues from the rounded state) and after the last token, which is
  * what is stored. Outputs come from the unrounded FP32 state.
+ * Arithmetic: FP32 for fp32 states. For bf16/fp16 states with dk = 128 and
+ * dv a multiple of 128 the chunked form runs on the tensor cores: the state,
+ * accumulation and rounding points stay FP32, the matrix products take TF32
+ * operands (within the 16-bit state's own rounding).
  * cu_seqlens   [B + 1] int32 device array, 0 <= cu_seqlens[b] <= cu_seqlens[b+1]
  *              <= total_tokens (otherwise GDN_DEVERR_SEQLEN and the sequence
  *              is skipped).
