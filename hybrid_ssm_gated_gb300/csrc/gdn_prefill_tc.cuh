@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
         // operand), T (an operand; first the products of the off-diagonal stages) and the inverse.
         unsigned char* sY = sKQ;                                        // [128 j][64 s], operand layout
         unsigned char* sT = sKQ + 128 * 64 * 4;                         // [64 t][64 s], operand layout
-        float* sM = reinterpret_cast<float*>(sT);                       // [3][16][16] stage products
+        float* sM = reinterpret_cast<float*>(sT);                       // [6][16][16] products B_IK
         float* sTi = reinterpret_cast<float*>(sKQ + 128 * 64 * 4 + 64 * 64 * 4);  // (I + A)^{-1}, [64][64]
         {
             float v[CH];
@@ -501,9 +501,27 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
             } else {
                 const int j = 32 * warp + lane;
                 tmem_ld<64>(tmem + lane_base + C_SKQ, v);
+                // the staged values by explicit shared-memory loads (16-bit inputs) and the decays four at a time
+                const uint32_t vrow = smem_addr(sD) + j * isz;
 #pragma unroll
-                for (int s_ = 0; s_ < CH; ++s_)
-                    v[s_] = (s_ < C ? load_elem(sD + s_ * ROWS * isz, j, in_dt) - seg[s_] * v[s_] : 0.f);
+                for (int s4 = 0; s4 < CH; s4 += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4*>(seg + s4);
+                    const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s_ = s4 + u;
+                        float vs;
+                        if (isz == 2) {
+                            uint16_t hraw;
+                            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hraw) : "r"(vrow + s_ * ROWS * 2));
+                            vs = in_dt == GDN_BF16 ? __uint_as_float(static_cast<uint32_t>(hraw) << 16)
+                                                   : __half2float(__ushort_as_half(hraw));
+                        } else {
+                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs) : "r"(vrow + s_ * ROWS * 4));
+                        }
+                        v[s_] = s_ < C ? vs - ev[u] * v[s_] : 0.f;
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < CH; i += 4)
                     *reinterpret_cast<float4*>(sY + op_off(j, i, 128)) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
@@ -530,38 +548,40 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
             }
         }
         __syncthreads();
-        // block row I: M_J = sum_{K=J}^{I-1} A[I][K] Tinv[K][J], then Tinv[I][J] = -Tinv[I][I] M_J (J < I)
+        // off-diagonal blocks: B_IK = Tinv[I][I] A[I][K] for every K < I at once, then block row by block row
+        // Tinv[I][J] = -sum_{K=J}^{I-1} B_IK Tinv[K][J] (J < I); B_IK at sM[(I (I - 1) / 2 + K) 256]
+        for (int o = tid; o < 6 * 256; o += THREADS) {
+            const int pr = o >> 8, r = (o >> 4) & 15, c = o & 15;
+            const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3), K = pr - I * (I - 1) / 2;
+            const float* drow = sTi + (16 * I + r) * 64 + 16 * I;
+            const float* acol = sA + (16 * I) * A_LD + 16 * K + c;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u4 = 0; u4 < 16; u4 += 4) {
+                const float4 d = *reinterpret_cast<const float4*>(drow + u4);
+                acc[0] = fmaf(d.x, acol[(u4 + 0) * A_LD], acc[0]);
+                acc[1] = fmaf(d.y, acol[(u4 + 1) * A_LD], acc[1]);
+                acc[2] = fmaf(d.z, acol[(u4 + 2) * A_LD], acc[2]);
+                acc[3] = fmaf(d.w, acol[(u4 + 3) * A_LD], acc[3]);
+            }
+            sM[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        __syncthreads();
         for (int I = 1; I < 4; ++I) {
             for (int o = tid; o < I * 256; o += THREADS) {
                 const int J = o >> 8, r = (o >> 4) & 15, c = o & 15;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int K = J; K < I; ++K) {
-                    const float* arow = sA + (16 * I + r) * A_LD + 16 * K;
+                    const float* brow = sM + (I * (I - 1) / 2 + K) * 256 + r * 16;
                     const float* tcol = sTi + (16 * K) * 64 + 16 * J + c;
 #pragma unroll
                     for (int s4 = 0; s4 < 16; s4 += 4) {
-                        const float4 av = *reinterpret_cast<const float4*>(arow + s4);
-                        acc[0] = fmaf(av.x, tcol[(s4 + 0) * 64], acc[0]);
-                        acc[1] = fmaf(av.y, tcol[(s4 + 1) * 64], acc[1]);
-                        acc[2] = fmaf(av.z, tcol[(s4 + 2) * 64], acc[2]);
-                        acc[3] = fmaf(av.w, tcol[(s4 + 3) * 64], acc[3]);
+                        const float4 bv = *reinterpret_cast<const float4*>(brow + s4);
+                        acc[0] = fmaf(bv.x, tcol[(s4 + 0) * 64], acc[0]);
+                        acc[1] = fmaf(bv.y, tcol[(s4 + 1) * 64], acc[1]);
+                        acc[2] = fmaf(bv.z, tcol[(s4 + 2) * 64], acc[2]);
+                        acc[3] = fmaf(bv.w, tcol[(s4 + 3) * 64], acc[3]);
                     }
-                }
-                sM[o] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            }
-            __syncthreads();
-            for (int o = tid; o < I * 256; o += THREADS) {
-                const int J = o >> 8, r = (o >> 4) & 15, c = o & 15;
-                const float* drow = sTi + (16 * I + r) * 64 + 16 * I;
-                const float* mcol = sM + J * 256 + c;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int u4 = 0; u4 < 16; u4 += 4) {
-                    const float4 d = *reinterpret_cast<const float4*>(drow + u4);
-                    acc[0] = fmaf(d.x, mcol[(u4 + 0) * 16], acc[0]);
-                    acc[1] = fmaf(d.y, mcol[(u4 + 1) * 16], acc[1]);
-                    acc[2] = fmaf(d.z, mcol[(u4 + 2) * 16], acc[2]);
-                    acc[3] = fmaf(d.w, mcol[(u4 + 3) * 16], acc[3]);
                 }
                 sTi[(16 * I + r) * 64 + 16 * J + c] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
             }
