@@ -131,18 +131,6 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
 template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-template <>
 __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(
