@@ -521,6 +521,22 @@ def fp32_alu_peak_tflops(dev) -> tuple[float, str]:
     return sms * 128 * 2 * mhz * 1e6 / 1e12, f"{sms} SMs x 128 x 2 x {mhz:.0f} MHz"
 
 
+def prefill_mma_flops(B: int, Hv: int, dv: int, tokens: int, interval: int = 64) -> int:
+    """MMA flops of the chunked tensor-core prefill for B sequences of `tokens` tokens: per chunk of 64 tokens
+    (the write-back interval dividing 64) and 128 state rows, S0 [K;Q]^T (128x128x128), [K;Q] K^T (128x64x128),
+    Y T^T and delta^T P^T (128x64x64 each), delta^T K~ (128x128x64), at 2 flops a multiply-add."""
+    chunks = B * Hv * (dv // 128) * ((tokens + min(64, interval) - 1) // min(64, interval))
+    return chunks * 2 * (128 * 128 * 128 + 128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+
+
+def prefill_bytes(B: int, Hk: int, Hv: int, dk: int, dv: int, tokens: int, state_bytes: int, in_bytes: int = 2,
+                  out_bytes: int = 4) -> int:
+    """Algorithmic HBM bytes of a prefill call: every token's q, k, v, a, b read and output written, and each
+    (sequence, head) state read once and written once."""
+    per_token = 2 * Hk * dk * in_bytes + Hv * dv * in_bytes + 2 * Hv * in_bytes + Hv * dv * out_bytes
+    return B * tokens * per_token + 2 * B * Hv * dv * dk * state_bytes
+
+
 def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
     """Prefill of 19 sequences of 2048 tokens (Hk=16, Hv=32, dk=dv=128, bf16 activations), state written
     back every 64 tokens, fp32 and bf16 state: tokens/s. The fp32 state runs the sequential kernel: its rate
@@ -545,10 +561,7 @@ def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
     out = torch.empty(total, w.Hv, w.dv, device=dev)
     peak, peak_note = fp32_alu_peak_tflops(dev)
     flops = 7 * w.dk * w.dv * w.Hv * total
-    # the chunked kernel's MMAs per chunk of 64 tokens and 128 state rows: S0 [K;Q]^T (128x128x128), [K;Q] K^T
-    # (128x64x128), Y T^T and delta^T P^T (128x64x64 each), delta^T K~ (128x128x64)
-    chunks = w.B * w.Hv * (w.dv // 128) * ((w.prefill_len + 63) // 64)
-    mma_flops = chunks * 2 * (128 * 128 * 128 + 128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+    mma_flops = prefill_mma_flops(w.B, w.Hv, w.dv, w.prefill_len)
     bf16_peak, bf16_note = 0.0, "MEASURED_PEAKS.json absent"
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -557,8 +570,6 @@ def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
         bf16_peak, bf16_note = FALLBACK_BF16_TFLOPS, "fallback"
     tf32_peak = bf16_peak * 1.1 / 2.25
     hbm_peak, _, _ = load_peaks()
-    in_b = 2
-    hbm_bytes = total * (2 * w.Hk * w.dk * in_b + w.Hv * w.dv * in_b + 2 * w.Hv * in_b + w.Hv * w.dv * 4)
     calls = max(5, args.steps // 200)
     for name, sdt in (("fp32", torch.float32), ("bf16", torch.bfloat16)):
         pool = (torch.randn(w.num_slots, w.Hv, w.dv, w.dk, generator=gen, device=dev) * 0.1).to(sdt)
@@ -566,8 +577,8 @@ def prefill_modes(modes, timed, args, world, dev, gen, err, stream) -> int:
                        calls, 3)
         entry = {"tokens_per_s": world * total * calls / (el / 1e3), "us_per_call": el / calls * 1e3,
                  "sequences": w.B, "tokens_per_sequence": w.prefill_len, "state_write_interval": 64}
-        state_bytes = 2 * w.B * w.Hv * w.dv * w.dk * pool.element_size()
-        gbs = (hbm_bytes + state_bytes) / (lm / 1e3) / 1e9
+        nbytes = prefill_bytes(w.B, w.Hk, w.Hv, w.dk, w.dv, w.prefill_len, pool.element_size())
+        gbs = nbytes / (lm / 1e3) / 1e9
         if name == "fp32":
             tf = flops / (lm / 1e3) / 1e12
             entry.update({"kernel": "prefill_kernel (sequential, FP32 FMA)", "bound": "alu", "alu_tflops": tf,

@@ -50,3 +50,20 @@ def test_mamba2_bytes():
     # the appended entry raw B, raw x and a record (656); the output 256; the pointers 16
     assert bench.mamba2_replay_unit_bytes(7, False, 4) == 32_768 + 7 * 528 + 32 + 128 + 2 + 656 + 256 + 16
     assert bench.mamba2_replay_unit_bytes(16, True, 2) == 2 * 16_384 + 16 * 528 + 162 + 656 + 256 + 16
+
+
+def test_prefill_counts():
+    # MMA flops of the tensor-core prefill, per chunk of 64 tokens and 128 state rows:
+    # 2 * (128*128*128 + 128*64*128 + 2 * 128*64*64 + 128*128*64) = 2 * 5,242,880 = 10,485,760;
+    # 19 sequences x 32 heads x 32 chunks of the 2048-token workload
+    assert bench.prefill_mma_flops(1, 1, 128, 64) == 10_485_760
+    assert bench.prefill_mma_flops(19, 32, 128, 2048) == 19 * 32 * 32 * 10_485_760 == 204_010_946_560
+    # a ragged last chunk counts as a chunk; dv = 256 is two row blocks; an interval of 16 makes chunks of 16
+    assert bench.prefill_mma_flops(1, 1, 128, 65) == 2 * 10_485_760
+    assert bench.prefill_mma_flops(1, 1, 256, 64) == 2 * 10_485_760
+    assert bench.prefill_mma_flops(1, 1, 128, 64, interval=16) == 4 * 10_485_760
+    # HBM bytes: per token q and k (2 * 16 * 128 * 2), v (32 * 128 * 2), a and b (2 * 32 * 2), the fp32
+    # output (32 * 128 * 4); per (sequence, head) the state read and written (2 * 128 * 128 * s)
+    per_token = 8_192 + 8_192 + 128 + 16_384
+    assert bench.prefill_bytes(1, 16, 32, 128, 128, 1, 4) == per_token + 2 * 32 * 65_536
+    assert bench.prefill_bytes(19, 16, 32, 128, 128, 2048, 2) == 19 * 2048 * per_token + 2 * 19 * 32 * 32_768
