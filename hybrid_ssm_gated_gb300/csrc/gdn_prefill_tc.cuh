@@ -382,31 +382,31 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
             const int n = 16 * warp + 8 * grp + rr;
             const bool key = n < 64;
             const int t = key ? n : n - 64;
-            float x[2][32];
+            float x[32];
             if (isz == 4) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    x[grp][4 * i] = __uint_as_float(xr[grp][i].x), x[grp][4 * i + 1] = __uint_as_float(xr[grp][i].y),
-                    x[grp][4 * i + 2] = __uint_as_float(xr[grp][i].z), x[grp][4 * i + 3] = __uint_as_float(xr[grp][i].w);
+                    x[4 * i] = __uint_as_float(xr[grp][i].x), x[4 * i + 1] = __uint_as_float(xr[grp][i].y),
+                    x[4 * i + 2] = __uint_as_float(xr[grp][i].z), x[4 * i + 3] = __uint_as_float(xr[grp][i].w);
             } else if (in_dt == GDN_BF16) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) Store<__nv_bfloat16>::unpack(xr[grp][i], x[grp] + 8 * i);
+                for (int i = 0; i < 4; ++i) Store<__nv_bfloat16>::unpack(xr[grp][i], x + 8 * i);
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) Store<__half>::unpack(xr[grp][i], x[grp] + 8 * i);
+                for (int i = 0; i < 4; ++i) Store<__half>::unpack(xr[grp][i], x + 8 * i);
             }
             float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ss = fmaf(x[grp][e], x[grp][e], ss);
+            for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
             ss += __shfl_xor_sync(FULL_MASK, ss, 8);
             ss += __shfl_xor_sync(FULL_MASK, ss, 16);
             const float sc = rsqrtf(ss + 1e-6f) * (key ? 1.f : p.q_scale);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[grp][e] = (x[grp][e] * sc);
+            for (int e = 0; e < 32; ++e) x[e] *= sc;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<float4*>(sKQ + op_off(n, 32 * qq + 4 * c, 128)) =
-                    make_float4(x[grp][4 * c], x[grp][4 * c + 1], x[grp][4 * c + 2], x[grp][4 * c + 3]);
+                    make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
             if (key) {
                 // K~ element (i, t): store k of the lane writes element e = 8 (k / 8) + ((k ^ key3) & 7), key3
                 // = 2 qq + rr / 4, so that the 32 lanes of a store hit 32 banks (bank: (e & 7) 4 + t & 3). The
@@ -415,21 +415,21 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
                 const float dk = t < C ? skt[t] : 0.f;
                 const int key3 = (2 * qq + (rr >> 2)) & 7;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[grp][e] = (x[grp][e] * dk);
+                for (int e = 0; e < 32; ++e) x[e] *= dk;
 #pragma unroll
                 for (int bit = 1; bit < 8; bit <<= 1) {
                     const bool sw = key3 & bit;
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (!(e & bit)) {
-                            const float a0 = x[grp][e], a1 = x[grp][e | bit];
-                            x[grp][e] = sw ? a1 : a0, x[grp][e | bit] = sw ? a0 : a1;
+                            const float a0 = x[e], a1 = x[e | bit];
+                            x[e] = sw ? a1 : a0, x[e | bit] = sw ? a0 : a1;
                         }
                 }
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
                     const int e = (k & ~7) | ((k ^ key3) & 7);
-                    *reinterpret_cast<float*>(sKT + op_off(32 * qq + e, t, 128)) = x[grp][k];
+                    *reinterpret_cast<float*>(sKT + op_off(32 * qq + e, t, 128)) = x[k];
                 }
             }
         }
@@ -579,10 +579,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
         for (int o = tid; o < 64 * 16; o += THREADS) {
             const int t = o >> 4, s4 = (o & 15) * 4;
             float4 v = *reinterpret_cast<const float4*>(sTi + t * 64 + s4);
-            v.x = s4 + 0 <= t ? (v.x * sbeta[s4 + 0]) : 0.f;
-            v.y = s4 + 1 <= t ? (v.y * sbeta[s4 + 1]) : 0.f;
-            v.z = s4 + 2 <= t ? (v.z * sbeta[s4 + 2]) : 0.f;
-            v.w = s4 + 3 <= t ? (v.w * sbeta[s4 + 3]) : 0.f;
+            v.x = s4 + 0 <= t ? v.x * sbeta[s4 + 0] : 0.f;
+            v.y = s4 + 1 <= t ? v.y * sbeta[s4 + 1] : 0.f;
+            v.z = s4 + 2 <= t ? v.z * sbeta[s4 + 2] : 0.f;
+            v.w = s4 + 3 <= t ? v.w * sbeta[s4 + 3] : 0.f;
             *reinterpret_cast<float4*>(sT + op_off(t, s4, 64)) = v;
         }
         fence_async_smem();
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(const Prefil
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4*>(sD + op_off(j, tb + i, 128)) =
-                    make_float4(v[i], (v[i + 1]), (v[i + 2]), (v[i + 3]));
+                    make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         }
         fence_async_smem();
         fence_before();
