@@ -92,6 +92,21 @@ def test_prefill_extreme_decays(sdt, d):
     _check_all(w, [40, 70, 17], wl.slots(w), 16, params=params)
 
 
+@pytest.mark.parametrize("sdt", ["bf16", "f16"])
+def test_prefill_tensor_core_shapes(sdt):
+    # d = 128 keys with 16-bit states take the tensor-core kernel: dv = 256 (two row blocks), GQA, ragged
+    # lengths, an interval that does not divide the 64-token chunks
+    w = wl.Workload("pftc", B=3, Hk=1, Hv=2, dk=128, dv=256, steps=1, state_dtype=sdt, in_dtype="bf16", seed=67)
+    _check_all(w, [70, 3, 130], wl.slots(w), 48)
+
+
+def test_prefill_tensor_core_padding_out_of_range_and_narrow_output():
+    w = wl.Workload("pftp", B=4, Hk=1, Hv=2, dk=128, dv=128, steps=1, state_dtype="bf16", in_dtype="bf16",
+                    num_slots=6, seed=68)
+    _check_all(w, [9, 20, 5, 12], np.array([4, -1, 11, 0], np.int32), 4, out_dtype="bf16",
+               expect_err=gdn.DEVERR_SLOT)
+
+
 def test_prefill_padding_out_of_range_and_narrow_output():
     w = wl.Workload("pfp", B=4, Hk=2, Hv=4, dk=64, dv=64, steps=1, state_dtype="f32", in_dtype="bf16", num_slots=6,
                     seed=63)
