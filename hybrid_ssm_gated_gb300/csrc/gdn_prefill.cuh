@@ -1,5 +1,8 @@
 // gdn_prefill.cuh -- prefill of the gated delta rule with a rounded state
-// write-back per chunk (gdn_prefill).
+// write-back per chunk (gdn_prefill), token by token on the FP32 pipe: the
+// kernel for FP32 states (exact FP32 arithmetic) and for shapes the chunked
+// tensor-core kernel (gdn_prefill_tc.cuh: 16-bit states, dk = 128, dv a
+// multiple of 128) does not take.
 //
 // Semantics (vLLM PR #52191 summary, section 实现拆解 items 3-4: the chunked
 // kernel works on an FP32 copy of the state within a chunk and writes it back,
